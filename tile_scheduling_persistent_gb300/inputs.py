@@ -1,0 +1,78 @@
+"""Seeded synthetic inputs and the named workloads.
+
+This module holds no attention arithmetic: it only draws the random tensors
+(Q, K, V, dO) that both the CUDA path and the CPU oracle consume, and lists
+the workload shapes.  O and LSE are *derived* inputs (a forward pass) and are
+produced by the caller.
+
+Recipe: one CPU ``torch.Generator`` seeded with ``seed``; fp32 standard
+normals drawn in the order Q, K, V, dO, each multiplied by its sigma and
+rounded to bfloat16 (round to nearest even, torch's ``.to(torch.bfloat16)``).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+SCHEDULE_IDS = {
+    "atomic_nondet": 0,
+    "serialized_ascending": 1,
+    "descending_q": 2,
+    "shift": 3,
+    "symmetric_shift": 4,
+}
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    causal: bool
+    B: int
+    Hq: int
+    Hkv: int
+    S: int
+    D: int
+    sigma_qkv: float
+    sigma_do: float
+    schedules: tuple
+
+
+WORKLOADS = {
+    "full_b1_h2_s512_d64": Workload(
+        "full_b1_h2_s512_d64", False, 1, 2, 2, 512, 64, 1.0, 1.0,
+        ("atomic_nondet", "serialized_ascending", "descending_q", "shift", "symmetric_shift")),
+    "full_b4_h16_s4096_d128": Workload(
+        "full_b4_h16_s4096_d128", False, 4, 16, 16, 4096, 128, 1.0, 1.0,
+        ("shift", "serialized_ascending", "atomic_nondet")),
+    "causal_b4_h16_s8192_d128": Workload(
+        "causal_b4_h16_s8192_d128", True, 4, 16, 16, 8192, 128, 1.0, 1.0,
+        ("descending_q", "symmetric_shift", "serialized_ascending", "atomic_nondet")),
+    "causal_b1_h32_s16384_d64": Workload(
+        "causal_b1_h32_s16384_d64", True, 1, 32, 32, 16384, 64, 1.0, 1.0,
+        ("symmetric_shift", "descending_q")),
+    "gqa_causal_b1_hq32_hkv8_s16384_d128": Workload(
+        "gqa_causal_b1_hq32_hkv8_s16384_d128", True, 1, 32, 8, 16384, 128, 0.5, 1e-2,
+        ("symmetric_shift", "descending_q", "shift", "serialized_ascending", "atomic_nondet")),
+}
+
+
+def make_qkvdo(B: int, Hq: int, Hkv: int, S: int, D: int, seed: int = 0,
+               sigma_qkv: float = 1.0, sigma_do: float = 1.0):
+    """Seeded bf16 (q, k, v, do) on the CPU, shapes [B,H,S,D]."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(int(seed))
+
+    def draw(h, sigma):
+        x = torch.randn((B, h, S, D), generator=g, dtype=torch.float32)
+        return (x * sigma).to(torch.bfloat16)
+
+    q = draw(Hq, sigma_qkv)
+    k = draw(Hkv, sigma_qkv)
+    v = draw(Hkv, sigma_qkv)
+    do = draw(Hq, sigma_do)
+    return q, k, v, do
+
+
+def make_workload_inputs(w: Workload, seed: int = 0):
+    return make_qkvdo(w.B, w.Hq, w.Hkv, w.S, w.D, seed, w.sigma_qkv, w.sigma_do)
