@@ -1,0 +1,410 @@
+"""Benchmark of the deterministic attention backward (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A step is one pass of the whole hot path on one batch of synthetic input:
+dash_attn_bwd (zero dq and counters, delta, cached schedule tables, the
+persistent kernel) followed by dash_dq_finalize.  ``value`` is the nominal
+backward TFLOP/s (10*S^2*D per query head, halved for causal) of the best
+deterministic schedule of the workload, inputs resident in HBM; the
+non-deterministic schedule is timed the same way for the det/nondet ratio.
+``e2e`` times the same public calls with the inputs copied from pinned host
+memory and the gradients copied back inside every step.
+
+``--impl reference`` times the fp64 CPU oracle (the only reference this
+method has) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_WORKLOAD = "full_b4_h16_s4096_d128"
+METRIC = "deterministic attn-bwd TFLOP/s & % of BF16 peak; det/nondet throughput ratio"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--schedule", default=None, help="deterministic schedule to report (default: best of the workload's)")
+    ap.add_argument("--impl", default="dash", choices=["dash", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def flops_nominal(B, Hq, S, D, causal):
+    """Nominal backward FLOPs: 10*S^2*D per query head, halved for causal."""
+    f = 10.0 * S * S * D * B * Hq
+    return f / 2 if causal else f
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["bf16_tflops"]), float(m["bf16_tflops_sustained"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        time.sleep(0.25)
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            if self.t:
+                self.t.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        busy = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(busy), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def gpu_inputs(w, seed, device):
+    """Seeded bf16 inputs; O and LSE from a plain fp32 PyTorch forward on the GPU
+    (input synthesis only, outside every timed region)."""
+    import torch
+    from tile_scheduling_persistent_gb300.inputs import make_qkvdo
+    q, k, v, do = (t.to(device) for t in make_qkvdo(w.B, w.Hq, w.Hkv, w.S, w.D, seed, w.sigma_qkv, w.sigma_do))
+    G = w.Hq // w.Hkv
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.Hq, w.S, dtype=torch.float32, device=device)
+    scale = 1.0 / math.sqrt(w.D)
+    rows = 2048
+    ar = torch.arange(w.S, device=device)
+    for b in range(w.B):
+        for h in range(w.Hq):
+            K = k[b, h // G].float()
+            V = v[b, h // G].float()
+            for r0 in range(0, w.S, rows):
+                s = (q[b, h, r0:r0 + rows].float() @ K.T) * scale
+                if w.causal:
+                    s.masked_fill_(ar[None, :] > ar[r0:r0 + rows, None], float("-inf"))
+                lse_blk = torch.logsumexp(s, dim=-1)
+                lse[b, h, r0:r0 + rows] = lse_blk
+                o[b, h, r0:r0 + rows] = (torch.exp(s - lse_blk[:, None]) @ V).to(torch.bfloat16)
+    torch.cuda.synchronize()
+    return q, k, v, o, do, lse
+
+
+def time_schedule(w, sched, tensors, outs, steps, warmup, stream, kernel_events=False):
+    """Returns (ms per step, mean kernel ms or None, launches per step)."""
+    import torch
+    from tile_scheduling_persistent_gb300 import dash
+    q, k, v, o, do, lse = tensors
+    dq, dqb, dk, dv = outs
+    evs = []
+
+    def step(i):
+        if kernel_events:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            dash.attn_bwd_debug(q, k, v, o, do, lse, dq, dk, dv, w.causal, sched, stream=stream,
+                                kernel_events=(e0, e1))
+            evs.append((e0, e1))
+        else:
+            dash.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, w.causal, sched, stream=stream)
+        dash.dq_finalize(dq, dqb, stream=stream)
+
+    for i in range(warmup):
+        step(i)
+    evs.clear()
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for i in range(steps):
+        step(i)
+    end.record(stream)
+    torch.cuda.synchronize()
+    ms = start.elapsed_time(end) / steps
+    kms = statistics.mean(a.elapsed_time(b) for a, b in evs) if evs else None
+    code, info = dash.get_status(stream)
+    if code != 0:
+        raise RuntimeError("device status %d %s" % (code, info))
+    return ms, kms, 3   # preprocess + persistent kernel + finalize
+
+
+def main_gpu(args):
+    import torch
+    from tile_scheduling_persistent_gb300 import dash
+    from tile_scheduling_persistent_gb300.inputs import WORKLOADS
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    w = WORKLOADS[args.workload]
+    dash.lib()
+    tensors = gpu_inputs(w, seed=rank, device=device)
+    dq = torch.empty(w.B, w.Hq, w.S, w.D, dtype=torch.float32, device=device)
+    dqb = torch.empty(dq.shape, dtype=torch.bfloat16, device=device)
+    dk = torch.empty(w.B, w.Hkv, w.S, w.D, dtype=torch.bfloat16, device=device)
+    dv = torch.empty_like(dk)
+    outs = (dq, dqb, dk, dv)
+    stream = torch.cuda.current_stream()
+    flop = flops_nominal(w.B, w.Hq, w.S, w.D, w.causal)
+    det = [s for s in w.schedules if s != "atomic_nondet"]
+    if args.schedule:
+        det = [args.schedule]
+
+    # pick the best deterministic schedule on a short untimed probe run
+    trial = {}
+    for s in det:
+        ms, _, _ = time_schedule(w, s, tensors, outs, 3, 2, stream)
+        trial[s] = ms
+    best = min(trial, key=trial.get)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # timed: the best deterministic schedule (whole step), clocks sampled during it
+    barrier()
+    with ClockSampler(local) as clk:
+        ms_det, _, lps = time_schedule(w, best, tensors, outs, args.steps, args.warmup, stream)
+    barrier()
+    ms_det = max_over_ranks(ms_det)
+    clocks = clk.summary()
+    # the dominant kernel alone (events around its launch, same stream)
+    _, kms_det, _ = time_schedule(w, best, tensors, outs, args.steps, args.warmup, stream, kernel_events=True)
+    ms_nd, kms_nd, _ = time_schedule(w, "atomic_nondet", tensors, outs, args.steps, args.warmup, stream,
+                                     kernel_events=True)
+    ms_nd = max_over_ranks(ms_nd)
+
+    # end to end through the public API: host inputs in, gradients out, every step
+    e2e = e2e_run(w, best, tensors, args.steps, args.warmup, stream)
+    e2e_ms = max_over_ranks(e2e["ms"])
+
+    burst, sustained, src = peaks()
+    value = world * flop / (ms_det * 1e-3) / 1e12
+    kach = flop / (kms_det * 1e-3) / 1e12
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_det, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D,
+                   "causal": w.causal, "schedule": best, "parallelism": "independent problems per GPU",
+                   "l2": "inputs larger than L2 (no flush)"},
+        "pct_of_bf16_peak": round(100.0 * value / world / burst, 2),
+        "det_nondet_ratio": round(ms_nd / ms_det, 4),
+        "nondet_tflops": round(world * flop / (ms_nd * 1e-3) / 1e12, 2),
+        "schedule_trials_ms": {k: round(v, 4) for k, v in trial.items()},
+        "roofline": {"bound": "tensor", "achieved": round(kach, 2), "peak": burst, "unit": "TFLOP/s",
+                     "frac": round(kach / burst, 4), "traffic": None,
+                     "kernel": "dash_bwd_kernel", "peak_source": src + " burst bf16 (cuBLAS)",
+                     "kernel_ms": round(kms_det, 4), "nondet_kernel_ms": round(kms_nd, 4)},
+        "clocks": clocks,
+        "e2e": {"value": round(world * flop / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e_ms, 4)},
+        "gpu_launches": lps * args.steps,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def e2e_run(w, sched, tensors, steps, warmup, stream):
+    import torch
+    from tile_scheduling_persistent_gb300 import dash
+    host = [t.cpu().pin_memory() for t in tensors]
+    dev = [torch.empty_like(t) for t in tensors]
+    dq = torch.empty(w.B, w.Hq, w.S, w.D, dtype=torch.float32, device=dev[0].device)
+    dqb = torch.empty(dq.shape, dtype=torch.bfloat16, device=dq.device)
+    dk = torch.empty(w.B, w.Hkv, w.S, w.D, dtype=torch.bfloat16, device=dq.device)
+    dv = torch.empty_like(dk)
+    out_host = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (dqb, dk, dv)]
+    h2d = sum(t.numel() * t.element_size() for t in host)
+    d2h = sum(t.numel() * t.element_size() for t in out_host)
+
+    def step():
+        for d, h in zip(dev, host):
+            d.copy_(h, non_blocking=True)
+        q, k, v, o, do, lse = dev
+        dash.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, w.causal, sched, stream=stream)
+        dash.dq_finalize(dq, dqb, stream=stream)
+        for h, d in zip(out_host, (dqb, dk, dv)):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return {"ms": a.elapsed_time(b) / steps, "h2d": h2d, "d2h": d2h}
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def _cpu_threads():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def oracle_sample_step(w, heads, seed=0):
+    """fp64 oracle backward on `heads` query heads of batch 0 (one key/value
+    head group at a time); returns (seconds, nominal FLOP of the sample)."""
+    import numpy as np  # noqa: F401
+    from oracle import attention as A
+    from tile_scheduling_persistent_gb300.inputs import make_qkvdo
+    G = w.Hq // w.Hkv
+    groups = max(1, heads // G)
+    q, k, v, do = make_qkvdo(1, groups * G, groups, w.S, w.D, seed, w.sigma_qkv, w.sigma_do)
+    o, lse = A.attn_fwd(q, k, v, w.causal, row_block=2048, workers=_cpu_threads())
+    t0 = time.perf_counter()
+    A.attn_bwd(q, k, v, o, do, lse, w.causal, row_block=2048, workers=_cpu_threads())
+    dt = time.perf_counter() - t0
+    return dt, flops_nominal(1, groups * G, w.S, w.D, w.causal)
+
+
+def cpu_baseline(w, budget_s):
+    G = w.Hq // w.Hkv
+    total_t = total_f = 0.0
+    heads = 0
+    while total_t < budget_s and heads < w.B * w.Hq:
+        dt, f = oracle_sample_step(w, G, seed=heads)
+        total_t += dt
+        total_f += f
+        heads += G
+    return {"value": round(total_f / total_t / 1e12, 6), "unit": "TFLOP/s", "cores": _cpu_threads(),
+            "kind": "oracle",
+            "sample": "%d of %d query heads (batch 0, S=%d, D=%d, %s), fp64 NumPy backward, %.1f s" % (
+                heads, w.B * w.Hq, w.S, w.D, "causal" if w.causal else "full", total_t)}
+
+
+def main_reference(args):
+    from tile_scheduling_persistent_gb300.inputs import WORKLOADS
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    w = WORKLOADS[args.workload]
+    G = w.Hq // w.Hkv
+    for _ in range(args.warmup):
+        oracle_sample_step(w, G)
+    times, flops = [], []
+    for i in range(args.steps):
+        dt, f = oracle_sample_step(w, G, seed=i)
+        times.append(dt)
+        flops.append(f)
+    value = sum(flops) / sum(times) / 1e12
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "TFLOP/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(1e3 * sum(times) / len(times), 3),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D,
+                   "causal": w.causal},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": _cpu_threads(), "kind": "oracle",
+                         "sample": "each step: %d query heads (one key/value group) of batch 0, fp64 backward" % G},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    a = parse()
+    if a.impl == "reference":
+        main_reference(a)
+    else:
+        main_gpu(a)

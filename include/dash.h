@@ -1,0 +1,229 @@
+/*
+ * dash.h -- C ABI of libdash.so: deterministic attention backward (dQ, dK, dV)
+ * under the DASH tile schedules, for one GB300 (sm_103a) GPU.
+ *
+ * Source of the method: "DASH: Deterministic Attention Scheduling for
+ * High-Throughput" (gist.science technical summary of arXiv 2601.21824),
+ * sections 1 (fixed dQ accumulation order), 2.1 (DAG model) and 2.2
+ * (descending Q-tile iteration, shift and symmetric shift scheduling); and
+ * the pwwt.cn write-up "DASH: how it changes deterministic LLM training",
+ * sections 2.2-2.3 (chain model, shift rotation, closed forms) and 3.1 (the
+ * release-side counter of an ordered reduction).
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ *  - Tensor pointers are DEVICE pointers owned by the caller, contiguous
+ *    row-major [B, H, S, D] (LSE and delta: [B, H, S]), 16-byte aligned.
+ *  - dash_bf16 is the raw 16-bit storage of a bfloat16 value.
+ *  - S must be a positive multiple of 128 (tiles are 128 x 128); D is 64 or
+ *    128; Hq must be a multiple of Hkv (query heads hq = g*G .. g*G+G-1 share
+ *    key/value head g, G = Hq / Hkv).
+ *  - LSE is the natural-log log-sum-exp of scale * Q K^T per query row with
+ *    scale = 1/sqrt(D) (the forward's statistic); masks are "full" or
+ *    top-left causal (key j visible to query i iff j <= i).
+ *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *    default stream) and returns a dash_status; errors never throw.
+ *  - Library-owned scratch (delta, per-tile semaphores, schedule tables, the
+ *    status word) lives in a workspace cached per (device, stream) and grown
+ *    on demand; dash_release_workspaces() frees it.  Calls on the same stream
+ *    are ordered; concurrent calls that share a stream from several host
+ *    threads are not supported.  Different devices/streams are independent.
+ */
+#ifndef DASH_H
+#define DASH_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t dash_bf16;
+typedef struct CUstream_st* dash_stream_t;
+
+typedef enum {
+    DASH_OK = 0,
+    DASH_ERR_ARG = -1,        /* invalid argument (null, misaligned, bad shape, unknown schedule) */
+    DASH_ERR_CUDA = -2,       /* a CUDA runtime/driver call failed */
+    DASH_ERR_LAUNCH = -3,     /* the persistent grid cannot be co-resident on this device */
+    DASH_ERR_TIMEOUT = -4,    /* device-side wait exceeded the timeout (reported by dash_get_status) */
+    DASH_ERR_DEADLOCK = -5,   /* a schedule table cannot complete (cycle or missing predecessor) */
+    DASH_ERR_NOMEM = -6,      /* workspace allocation failed */
+    DASH_ERR_DEVICE = -7      /* device is not sm_103 / lacks the needed shared memory */
+} dash_status;
+
+typedef enum {
+    DASH_SCHED_ATOMIC_NONDET = 0,        /* unordered fp32 atomics: fast, NOT reproducible */
+    DASH_SCHED_SERIALIZED_ASCENDING = 1, /* ascending Q visits, ascending-KV accumulation order */
+    DASH_SCHED_DESCENDING_Q = 2,         /* descending Q visits, ascending-KV accumulation order */
+    DASH_SCHED_SHIFT = 3,                /* cyclic Q rotation per KV tile, model-time order */
+    DASH_SCHED_SYMMETRIC_SHIFT = 4       /* causal: KV pairs (j, n-1-j), two phases; full mask = SHIFT */
+} dash_schedule;
+
+/*
+ * dash_attn_bwd_preprocess -- delta[b,h,s] = sum_d dO[b,h,s,d] * O[b,h,s,d].
+ *
+ * The per-row statistic of the softmax backward (dS = P o (dP - delta)).
+ * o, dO: bf16 [B,Hq,S,D]; delta: fp32 [B,Hq,S] written by the call.  Each row
+ * is summed in fp32 in one fixed order, so the result is bitwise
+ * reproducible.  Returns DASH_ERR_ARG on null/misaligned pointers or bad
+ * sizes (S need not be a multiple of 128 here), DASH_ERR_CUDA on launch
+ * failure.
+ */
+int dash_attn_bwd_preprocess(const dash_bf16* o, const dash_bf16* dO, float* delta,
+                             int B, int Hq, int S, int D, dash_stream_t stream);
+
+/*
+ * dash_attn_bwd -- the deterministic attention backward pass.
+ *
+ * Inputs: q, o, dO bf16 [B,Hq,S,D]; k, v bf16 [B,Hkv,S,D]; lse fp32 [B,Hq,S].
+ * Outputs:
+ *   dq  fp32 [B,Hq,S,D] -- the fp32 dQ accumulator.  The library zeroes it
+ *       and leaves the final, scaled dQ in it (dash_dq_finalize rounds it to
+ *       bf16).  Each dQ tile (128 rows of one head) is the fp32 sum of its
+ *       KV-tile partials added in the order the schedule fixes.
+ *   dk, dv bf16 [B,Hkv,S,D] -- accumulated on chip per KV tile over the
+ *       tile's pairs in the schedule's visit order and over the query heads
+ *       of its group in ascending head order; rounded to nearest even.
+ * schedule: a dash_schedule value.  causal: 0 (full) or 1 (top-left causal).
+ *
+ * For every schedule except DASH_SCHED_ATOMIC_NONDET the three outputs are
+ * bitwise identical across runs on the same device model and SM count,
+ * whatever the launch timing.  The call computes delta itself (o is an
+ * argument), zeroes dq, builds or reuses the schedule tables, and launches
+ * one persistent CTA per SM (cooperative launch).
+ *
+ * Errors: DASH_ERR_ARG (null or non-16-byte-aligned pointer, S % 128 != 0,
+ * D not in {64,128}, Hq % Hkv != 0, non-positive sizes, unknown schedule or
+ * causal flag), DASH_ERR_DEVICE, DASH_ERR_LAUNCH, DASH_ERR_NOMEM,
+ * DASH_ERR_CUDA.  A device-side wait that exceeds the timeout does not hang:
+ * the kernel stops, leaves dq/dk/dv undefined and records DASH_ERR_TIMEOUT,
+ * which dash_get_status reports.
+ */
+int dash_attn_bwd(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v,
+                  const dash_bf16* o, const dash_bf16* dO, const float* lse,
+                  float* dq, dash_bf16* dk, dash_bf16* dv,
+                  int B, int Hq, int Hkv, int S, int D, int causal, int schedule,
+                  dash_stream_t stream);
+
+/*
+ * dash_dq_finalize -- dq[i] = bf16_round_to_nearest_even(dq_accum[i]) for
+ * i < numel.  dq_accum fp32, dq bf16; both device pointers, 16-byte aligned.
+ * Returns DASH_ERR_ARG / DASH_ERR_CUDA.
+ */
+int dash_dq_finalize(const float* dq_accum, dash_bf16* dq, size_t numel, dash_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Status and configuration
+ * ------------------------------------------------------------------------- */
+
+/*
+ * dash_get_status -- synchronizes `stream` and reports the device status of
+ * the last dash_attn_bwd on (current device, stream): *code = DASH_OK or
+ * DASH_ERR_TIMEOUT; info[0..3] = {b*Hq+hq, Q tile, expected turn, role} of
+ * the first wait that timed out (role 0 reducer, 1 producer, 2 MMA,
+ * 3 softmax/dS).  info may be NULL.  Returns DASH_OK or DASH_ERR_CUDA.
+ */
+int dash_get_status(dash_stream_t stream, int* code, int* info);
+
+/* Timeout of every device-side wait, in ns (default 2e9).  Returns DASH_OK. */
+int dash_set_timeout_ns(uint64_t ns);
+
+/* Frees every cached workspace of the calling process (all devices).  The
+ * caller must ensure no dash call is in flight.  Returns DASH_OK. */
+int dash_release_workspaces(void);
+
+/* *P = number of persistent CTAs (one per SM) dash_attn_bwd uses on `device`;
+ * the static schedules' accumulation order depends on it. */
+int dash_num_ctas(int device, int* P);
+
+/* ---------------------------------------------------------------------------
+ * Schedule simulator (host only, no GPU needed)
+ *
+ * The DAG model of the DASH summary, section 2.1: each pair (KV tile j,
+ * Q tile i) is a compute of cost c followed by a reduce of cost r; the pairs
+ * of one task run back to back on one SM; the reduces into one dQ tile follow
+ * the accumulation order.  Static schedules (shift, symmetric shift) give
+ * task k to SM k % P; the others dispatch greedily in task order.
+ * ------------------------------------------------------------------------- */
+
+/*
+ * dash_sim_schedule -- simulate `schedule` for the shape (B,Hq,Hkv,n tiles
+ * per head, causal) on P SMs.
+ *   makespan (out, may be NULL): the critical-path length.
+ *   turn_order (out, may be NULL): int32 [B*Hq*n][n]; row ((b*Hq+hq)*n+i)
+ *     lists the KV tiles accumulated into dQ tile i of head (b,hq), in order,
+ *     padded with -1 (for DASH_SCHED_ATOMIC_NONDET: the order of the
+ *     simulated reduce completions).
+ *   num_tasks (out, may be NULL).
+ * Returns DASH_OK, DASH_ERR_ARG, DASH_ERR_NOMEM or DASH_ERR_DEADLOCK.
+ */
+int dash_sim_schedule(int schedule, int causal, int B, int Hq, int Hkv, int n, int P,
+                      double c, double r, double* makespan, int32_t* turn_order,
+                      int64_t* num_tasks);
+
+/*
+ * dash_sim_check_ranks -- would the kernel complete with this accumulation
+ * table?  ranks: host uint16 [B*Hq*n][n], rank of KV tile j's partial in dQ
+ * tile i (entries of masked pairs are ignored).  The visit lists and SM
+ * assignment are those of `schedule` on P SMs.  Returns DASH_OK if every
+ * tile's ranks are exactly 0..m-1 and the chain + order DAG is acyclic,
+ * DASH_ERR_DEADLOCK otherwise, DASH_ERR_ARG on bad input.
+ */
+int dash_sim_check_ranks(int schedule, int causal, int B, int Hq, int Hkv, int n, int P,
+                         const uint16_t* ranks);
+
+/* ---------------------------------------------------------------------------
+ * Debug and test hooks (used by the test-suite; not needed for normal use)
+ * ------------------------------------------------------------------------- */
+
+typedef struct {
+    /* device int32 [B*Hq*n][n] or NULL: slot k of dQ tile t receives the KV
+     * index of the k-th partial actually added (log written as it happens). */
+    int32_t* order_log;
+    /* device fp32 [B*Hq*n*n][128][D] or NULL: the fp32 dQ partial of pair
+     * (b,hq,i,j) at index ((b*Hq+hq)*n+i)*n+j, as produced by the MMA. */
+    float* dq_partials;
+    /* device int32 [P] or NULL: worker slot used by CTA blockIdx.x (a
+     * permutation of 0..P-1). */
+    const int32_t* cta_perm;
+    /* device int64 [P] or NULL: ns each worker slot waits before starting. */
+    const int64_t* start_delay_ns;
+    /* host uint16 [B*Hq*n][n] or NULL: replaces the accumulation ranks of a
+     * deterministic schedule (checked by dash_sim_check_ranks first unless
+     * skip_table_check is nonzero). */
+    const uint16_t* ranks_host;
+    int skip_table_check;
+    /* two cudaEvent_t or NULL: recorded on `stream` immediately before and
+     * after the persistent kernel's launch (for timing that kernel alone). */
+    void* kernel_event_begin;
+    void* kernel_event_end;
+} dash_debug_opts;
+
+/* dash_attn_bwd with debug hooks; same arguments and errors, plus
+ * DASH_ERR_DEADLOCK when a supplied table fails the simulator check. */
+int dash_attn_bwd_debug(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v,
+                        const dash_bf16* o, const dash_bf16* dO, const float* lse,
+                        float* dq, dash_bf16* dk, dash_bf16* dv,
+                        int B, int Hq, int Hkv, int S, int D, int causal, int schedule,
+                        dash_stream_t stream, const dash_debug_opts* opts);
+
+/*
+ * dash_debug_tile_probe -- one (KV tile, Q tile) pair computed by the same
+ * device building blocks as the persistent kernel, one CTA, no pipelining:
+ * k, v, q, dO bf16 [128][D]; lse, delta fp32 [128]; outputs fp32 [128][128]
+ * sT (S^T), pT (P^T), dpT (dP^T), dsT (dS^T incl. scale), and fp32 [128][D]
+ * dv (P^T dO), dk (dS^T Q), dq (dS K).  diag=1 applies the causal mask of a
+ * diagonal tile.  Synchronous.  For unit tests of the MMA operand layouts.
+ */
+int dash_debug_tile_probe(const dash_bf16* k, const dash_bf16* v, const dash_bf16* q,
+                          const dash_bf16* dO, const float* lse, const float* delta,
+                          int D, int diag, float* sT, float* pT, float* dpT, float* dsT,
+                          float* dv, float* dk, float* dq);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DASH_H */

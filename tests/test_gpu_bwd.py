@@ -1,0 +1,227 @@
+"""GPU parity, determinism and ordering tests of dash_attn_bwd (small shapes).
+
+Every comparison is against the fp64 CPU oracle (parity) or against the
+kernel itself / the schedule simulator (bitwise determinism, order logs).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as A
+from tile_scheduling_persistent_gb300 import dash
+
+from gpu_helpers import check, make_case, run, same_bits, sim_turns
+
+pytestmark = pytest.mark.gpu
+
+SCHEDS = ["atomic_nondet", "serialized_ascending", "descending_q", "shift", "symmetric_shift"]
+ORDERED = SCHEDS[1:]
+
+SHAPES = {
+    # name: (B, Hq, Hkv, S, D, causal)
+    "full_s512_d64": (1, 2, 2, 512, 64, False),        # the small workload: n = 4 KV tiles
+    "causal_s512_d64": (1, 2, 2, 512, 64, True),
+    "full_s384_d128_gqa": (1, 4, 2, 384, 128, False),  # odd n = 3, GQA 2:1
+    "causal_s384_d128_gqa": (1, 4, 2, 384, 128, True),
+    "causal_s640_d64_gqa": (2, 2, 1, 640, 64, True),   # n = 5, B = 2
+    "full_s256_d128": (1, 2, 2, 256, 128, False),
+    "causal_s1024_d128": (1, 3, 3, 1024, 128, True),   # n = 8
+    "causal_s128_d64": (1, 1, 1, 128, 64, True),       # a single (diagonal) tile
+}
+
+_cases = {}
+
+
+def case(name):
+    if name not in _cases:
+        _cases[name] = make_case(*SHAPES[name])
+    return _cases[name]
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+@pytest.mark.parametrize("sched", SCHEDS)
+def test_parity(name, sched):
+    c = case(name)
+    dq, dqb, dk, dv = run(c, sched)
+    dq_ref, dk_ref, dv_ref, _ = c.ref
+    check("dq", dqb, dq_ref)
+    check("dk", dk, dk_ref)
+    check("dv", dv, dv_ref)
+    # the fp32 accumulator itself is much closer than the bf16 output
+    check("dq_fp32", dq, dq_ref, rel_tol=5e-3, abs_tol=2e-2)
+
+
+@pytest.mark.parametrize("name", ["full_s512_d64", "causal_s384_d128_gqa", "causal_s1024_d128"])
+@pytest.mark.parametrize("sched", ORDERED)
+def test_bitwise_reproducible_20_runs(name, sched):
+    c = case(name)
+    first = run(c, sched)
+    for _ in range(19):
+        again = run(c, sched)
+        for a, b in zip(first, again):
+            assert same_bits(a, b)
+
+
+def test_ascending_and_descending_share_dq_bits():
+    for name in ("full_s512_d64", "causal_s640_d64_gqa", "causal_s1024_d128"):
+        c = case(name)
+        a = run(c, "serialized_ascending")
+        d = run(c, "descending_q")
+        assert same_bits(a[0], d[0])
+
+
+def test_symmetric_shift_is_shift_on_full_masks():
+    for name in ("full_s512_d64", "full_s384_d128_gqa"):
+        c = case(name)
+        a = run(c, "shift")
+        b = run(c, "symmetric_shift")
+        for x, y in zip(a, b):
+            assert same_bits(x, y)
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+@pytest.mark.parametrize("sched", ORDERED)
+def test_order_log_matches_simulator(name, sched):
+    c = case(name)
+    log = torch.full((c.B * c.Hq * c.n, c.n), -1, dtype=torch.int32, device="cuda")
+    run(c, sched, order_log=log)
+    np.testing.assert_array_equal(log.cpu().numpy(), sim_turns(c, sched))
+
+
+@pytest.mark.parametrize("sched", ORDERED + ["atomic_nondet"])
+def test_partials_resummed_in_logged_order_equal_accumulator(sched):
+    # Every fp32 partial the MMA produced, added on the CPU in fp32 in the
+    # logged order, must give the accumulator bit for bit.
+    c = case("full_s512_d64")
+    n, D = c.n, c.D
+    tiles = c.B * c.Hq * n
+    log = torch.full((tiles, n), -1, dtype=torch.int32, device="cuda")
+    parts = torch.zeros(tiles * n, 128, D, dtype=torch.float32, device="cuda")
+    dq, _, _, _ = run(c, sched, order_log=log, dq_partials=parts)
+    log = log.cpu().numpy()
+    parts = parts.cpu().numpy().reshape(tiles, n, 128, D)
+    acc = dq.cpu().numpy().reshape(tiles, 128, D)
+    if sched != "atomic_nondet":
+        np.testing.assert_array_equal(log, sim_turns(c, sched))
+    for t in range(tiles):
+        s = np.zeros((128, D), np.float32)
+        for j in log[t]:
+            s = (s + parts[t, j]).astype(np.float32)
+        if sched == "atomic_nondet":
+            np.testing.assert_allclose(s, acc[t], rtol=1e-5, atol=1e-6)
+        else:
+            np.testing.assert_array_equal(s.view(np.int32), acc[t].view(np.int32))
+
+
+@pytest.mark.parametrize("sched", ORDERED)
+def test_launch_perturbations_keep_bits(sched):
+    c = case("causal_s1024_d128")
+    base = run(c, sched)
+    P = dash.num_ctas()
+    g = torch.Generator().manual_seed(7)
+    perm = torch.randperm(P, generator=g).to(torch.int32).cuda()
+    delays = (torch.randint(0, 200_000, (P,), generator=g)).to(torch.int64).cuda()
+    for kw in ({"cta_perm": perm}, {"start_delay_ns": delays}, {"cta_perm": perm, "start_delay_ns": delays}):
+        got = run(c, sched, **kw)
+        for a, b in zip(base, got):
+            assert same_bits(a, b)
+    # another stream, and a busy kernel running concurrently on a third stream
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    with torch.cuda.stream(s2):
+        x = torch.randn(4096, 4096, device="cuda")
+        for _ in range(4):
+            x = x @ x
+            x = x / x.norm()
+    with torch.cuda.stream(s1):
+        got = run(c, sched, stream=s1)
+    torch.cuda.synchronize()
+    for a, b in zip(base, got):
+        assert same_bits(a, b)
+
+
+def test_atomic_nondet_is_within_tolerance_and_may_differ():
+    c = case("causal_s1024_d128")
+    runs = [run(c, "atomic_nondet")[0] for _ in range(5)]
+    spread = max(float((r - runs[0]).abs().max()) for r in runs)
+    assert spread < 1e-3      # recorded, not required to be zero
+
+
+def test_preprocess_delta():
+    c = case("causal_s384_d128_gqa")
+    delta = torch.empty(c.B, c.Hq, c.S, dtype=torch.float32, device="cuda")
+    dash.attn_bwd_preprocess(c.o, c.do, delta)
+    torch.cuda.synchronize()
+    ref = A.attn_bwd_delta(c.o.float().cpu(), c.do.float().cpu())
+    np.testing.assert_allclose(delta.cpu().numpy(), ref, rtol=1e-5, atol=1e-5)
+    again = torch.empty_like(delta)
+    dash.attn_bwd_preprocess(c.o, c.do, again)
+    assert same_bits(delta, again)
+
+
+def test_finalize_round_to_nearest_even():
+    g = torch.Generator().manual_seed(3)
+    x = torch.randn(1 << 16 | 5, generator=g) * 10
+    special = torch.tensor([0.0, -0.0, 1.0 + 2 ** -8, 1.0 + 3 * 2 ** -8, -(1.0 + 2 ** -8), float("inf"),
+                            -float("inf"), 3.0e38, 1e-40, 65504.0, 2 ** -126, 1.00390625])
+    x = torch.cat([x, special])
+    src = x.cuda()
+    dst = torch.empty(src.shape, dtype=torch.bfloat16, device="cuda")
+    dash.dq_finalize(src, dst)
+    torch.cuda.synchronize()
+    want = x.to(torch.bfloat16)
+    assert torch.equal(dst.cpu().view(torch.int16), want.view(torch.int16))
+
+
+def test_missing_predecessor_times_out_and_context_survives():
+    c = case("causal_s512_d64")
+    P = dash.num_ctas()
+    _, turns, _ = dash.sim_schedule("shift", c.causal, c.B, c.Hq, c.Hkv, c.n, P)
+    ranks = np.full(turns.shape, 0xFFFF, np.uint16)
+    for t in range(turns.shape[0]):
+        for r, j in enumerate(turns[t]):
+            if j >= 0:
+                ranks[t, j] = r
+    bad = ranks.copy()
+    t = c.n - 1                                   # last tile of head 0 has n contributors
+    bad[t, turns[t, 1]] = 7                       # rank 1 never arrives
+    assert dash.sim_check_ranks("shift", c.causal, c.B, c.Hq, c.Hkv, c.n, P, bad) == dash.ERR_DEADLOCK
+    dq, dk, dv = (torch.empty(c.B, c.Hq, c.S, c.D, dtype=torch.float32, device="cuda"),
+                  torch.empty(c.B, c.Hkv, c.S, c.D, dtype=torch.bfloat16, device="cuda"),
+                  torch.empty(c.B, c.Hkv, c.S, c.D, dtype=torch.bfloat16, device="cuda"))
+    # rejected on the host by the simulator check
+    with pytest.raises(dash.DashError) as e:
+        dash.attn_bwd_debug(c.q, c.k, c.v, c.o, c.do, c.lse, dq, dk, dv, c.causal, "shift", ranks_host=bad)
+    assert e.value.code == dash.ERR_DEADLOCK
+    # forced onto the device: the bounded wait runs out and reports, no hang
+    dash.set_timeout_ns(20_000_000)
+    try:
+        dash.attn_bwd_debug(c.q, c.k, c.v, c.o, c.do, c.lse, dq, dk, dv, c.causal, "shift", ranks_host=bad,
+                            skip_table_check=True)
+        code, info = dash.get_status()
+        assert code == dash.ERR_TIMEOUT
+        assert info[3] in (0, 1, 2, 3)
+    finally:
+        dash.set_timeout_ns(2_000_000_000)
+    # the context is still usable and the good table gives the normal result
+    good = run(c, "shift", ranks_host=ranks)
+    ref = run(c, "shift")
+    for a, b in zip(good, ref):
+        assert same_bits(a, b)
+
+
+def test_invalid_arguments_on_device():
+    c = case("full_s512_d64")
+    dq, dk, dv = (torch.empty(1, 2, 512, 64, dtype=torch.float32, device="cuda"),
+                  torch.empty(1, 2, 512, 64, dtype=torch.bfloat16, device="cuda"),
+                  torch.empty(1, 2, 512, 64, dtype=torch.bfloat16, device="cuda"))
+    L = dash.lib()
+    import ctypes
+    p = lambda t: ctypes.c_void_p(t.data_ptr())  # noqa: E731
+    s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    base = [p(c.q), p(c.k), p(c.v), p(c.o), p(c.do), p(c.lse), p(dq), p(dk), p(dv)]
+    assert L.dash_attn_bwd(*base, 1, 2, 2, 512, 64, 0, 9, s) == dash.ERR_ARG
+    assert L.dash_attn_bwd(*base, 1, 2, 2, 500, 64, 0, 3, s) == dash.ERR_ARG
+    mis = list(base)
+    mis[0] = ctypes.c_void_p(c.q.data_ptr() + 2)
+    assert L.dash_attn_bwd(*mis, 1, 2, 2, 512, 64, 0, 3, s) == dash.ERR_ARG
+    assert dash.num_ctas() >= 100

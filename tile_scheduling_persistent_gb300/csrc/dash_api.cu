@@ -1,0 +1,350 @@
+// dash_api.cu -- the C ABI of libdash.so (declared in include/dash.h):
+// argument validation, the per-(device, stream) workspace, tensor maps and
+// the launch sequence  tables (cached) -> zero dq / counters -> delta ->
+// persistent backward.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+#include <atomic>
+#include <map>
+#include <mutex>
+#include <utility>
+#include <vector>
+
+#include "../../include/dash.h"
+#include "dash_bwd.cuh"
+#include "dash_internal.h"
+#include "dash_schedule.h"
+
+namespace dash {
+
+namespace {
+
+std::atomic<unsigned long long> g_timeout_ns{2000000000ull};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// Growable device buffer.
+struct DevBuf {
+    void* p = nullptr;
+    size_t cap = 0;
+    int ensure(size_t bytes) {
+        if (bytes <= cap) return 0;
+        if (p) cudaFree(p);
+        p = nullptr;
+        cap = 0;
+        size_t want = bytes < 4096 ? 4096 : bytes;
+        if (cudaMalloc(&p, want) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return -6;
+        }
+        cap = want;
+        return 0;
+    }
+    void release() {
+        if (p) cudaFree(p);
+        p = nullptr;
+        cap = 0;
+    }
+};
+
+// ints layout: [0..7] status, [8] task counter, [9] abort, [16 .. 16+T) sem, [16+T .. 16+2T) log cursors
+constexpr int kIntHeader = 16;
+
+struct Workspace {
+    DevBuf delta, ints, ranks, time, task_start, dbg_ranks;
+    long long table_key[8] = {-1, -1, -1, -1, -1, -1, -1, -1};
+    void release() {
+        delta.release();
+        ints.release();
+        ranks.release();
+        time.release();
+        task_start.release();
+        dbg_ranks.release();
+        for (auto& k : table_key) k = -1;
+    }
+};
+
+std::mutex g_mu;
+std::map<std::pair<int, uintptr_t>, Workspace*>& workspaces() {
+    static auto* m = new std::map<std::pair<int, uintptr_t>, Workspace*>();
+    return *m;
+}
+
+Workspace* get_ws(int dev, cudaStream_t s) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto key = std::make_pair(dev, (uintptr_t)s);
+    auto& m = workspaces();
+    auto it = m.find(key);
+    if (it != m.end()) return it->second;
+    Workspace* w = new Workspace();
+    m[key] = w;
+    return w;
+}
+
+bool aligned16(const void* p) { return p && (((uintptr_t)p) & 15u) == 0; }
+
+int check_device(int* dev_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DASH_ERR_CUDA;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return DASH_ERR_CUDA;
+    if (major != 10 || minor != 3) return DASH_ERR_DEVICE;
+    *dev_out = dev;
+    return DASH_OK;
+}
+
+int validate_shape(int B, int Hq, int Hkv, int S, int D, int causal, int schedule) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0) return DASH_ERR_ARG;
+    if (S % 128 != 0) return DASH_ERR_ARG;
+    if (D != 64 && D != 128) return DASH_ERR_ARG;
+    if (Hq % Hkv != 0) return DASH_ERR_ARG;
+    if (causal != 0 && causal != 1) return DASH_ERR_ARG;
+    if (schedule < 0 || schedule > 4) return DASH_ERR_ARG;
+    if ((long long)B * Hq * S >= (1ll << 31)) return DASH_ERR_ARG;
+    if (S / 128 > 65535) return DASH_ERR_ARG;
+    return DASH_OK;
+}
+
+int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const dash_bf16* o, const dash_bf16* dO,
+             const float* lse, float* dq, dash_bf16* dk, dash_bf16* dv, int B, int Hq, int Hkv, int S, int D,
+             int causal, int schedule, cudaStream_t stream, const dash_debug_opts* dbg) {
+    const void* ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return DASH_ERR_ARG;
+    int rc = validate_shape(B, Hq, Hkv, S, D, causal, schedule);
+    if (rc) return rc;
+    int dev = 0;
+    if ((rc = check_device(&dev))) return rc;
+    int P = 0;
+    rc = bwd_max_ctas(D, dev, &P);
+    if (rc == -3) return DASH_ERR_LAUNCH;
+    if (rc) return DASH_ERR_CUDA;
+
+    const int n = S / 128;
+    const Shape sh{B, Hq, Hkv, n, Hq / Hkv, causal, schedule};
+    const long long tiles = (long long)B * Hq * n;
+    const long long entries = tiles * n;
+    const long long ntasks = num_tasks(sh);
+    const bool use_table = dbg && dbg->ranks_host;
+    if (use_table && !is_static(schedule)) return DASH_ERR_ARG;
+    if (use_table && !dbg->skip_table_check &&
+        dash_sim_check_ranks(schedule, causal, B, Hq, Hkv, n, P, dbg->ranks_host) != DASH_OK)
+        return DASH_ERR_DEADLOCK;
+
+    Workspace* ws = get_ws(dev, stream);
+    if (ws->delta.ensure((size_t)tiles * 128 * sizeof(float)) ||
+        ws->ints.ensure((size_t)(kIntHeader + 2 * tiles) * sizeof(int)))
+        return DASH_ERR_NOMEM;
+
+    const uint16_t* ranks = nullptr;
+    if (use_table) {
+        if (ws->dbg_ranks.ensure((size_t)entries * sizeof(uint16_t))) return DASH_ERR_NOMEM;
+        if (cudaMemcpyAsync(ws->dbg_ranks.p, dbg->ranks_host, (size_t)entries * sizeof(uint16_t),
+                            cudaMemcpyHostToDevice, stream) != cudaSuccess)
+            return DASH_ERR_CUDA;
+        ranks = (const uint16_t*)ws->dbg_ranks.p;
+    } else if (is_static(schedule)) {
+        const long long key[8] = {B, Hq, Hkv, n, causal, is_symmetric(sh) ? kSymmetric : kShift, P, 0};
+        if (memcmp(key, ws->table_key, sizeof(key)) != 0) {
+            if (ws->ranks.ensure((size_t)entries * sizeof(uint16_t)) ||
+                ws->time.ensure((size_t)entries * sizeof(uint32_t)) ||
+                ws->task_start.ensure((size_t)ntasks * sizeof(uint32_t)))
+                return DASH_ERR_NOMEM;
+            if (launch_build_ranks(B, Hq, Hkv, n, causal, schedule, P, (uint16_t*)ws->ranks.p,
+                                   (uint32_t*)ws->time.p, (uint32_t*)ws->task_start.p, stream))
+                return DASH_ERR_CUDA;
+            memcpy(ws->table_key, key, sizeof(key));
+        }
+        ranks = (const uint16_t*)ws->ranks.p;
+    }
+
+    int* ints = (int*)ws->ints.p;
+    if (cudaMemsetAsync(ints, 0, (size_t)(kIntHeader + 2 * tiles) * sizeof(int), stream) != cudaSuccess ||
+        cudaMemsetAsync(dq, 0, (size_t)tiles * 128 * D * sizeof(float), stream) != cudaSuccess)
+        return DASH_ERR_CUDA;
+    if (launch_preprocess(o, dO, (float*)ws->delta.p, tiles * 128, D, stream)) return DASH_ERR_CUDA;
+
+    BwdParams prm;
+    memset(&prm, 0, sizeof(prm));
+    if (make_tmap_2d(&prm.tm_q, q, (long long)B * Hq * S, D) || make_tmap_2d(&prm.tm_k, k, (long long)B * Hkv * S, D) ||
+        make_tmap_2d(&prm.tm_v, v, (long long)B * Hkv * S, D) || make_tmap_2d(&prm.tm_do, dO, (long long)B * Hq * S, D))
+        return DASH_ERR_CUDA;
+    prm.lse = lse;
+    prm.delta = (const float*)ws->delta.p;
+    prm.dq = dq;
+    prm.dk = (__nv_bfloat16*)dk;
+    prm.dv = (__nv_bfloat16*)dv;
+    prm.ranks = ranks;
+    prm.status = ints;
+    prm.task_counter = ints + 8;
+    prm.abort_flag = ints + 9;
+    prm.sem = ints + kIntHeader;
+    prm.logcnt = ints + kIntHeader + tiles;
+    if (dbg) {
+        prm.order_log = dbg->order_log;
+        prm.partials = dbg->dq_partials;
+        prm.cta_perm = dbg->cta_perm;
+        prm.delay_ns = dbg->start_delay_ns;
+    }
+    prm.timeout_ns = g_timeout_ns.load();
+    prm.ntasks = ntasks;
+    prm.B = B;
+    prm.Hq = Hq;
+    prm.Hkv = Hkv;
+    prm.S = S;
+    prm.n = n;
+    prm.G = Hq / Hkv;
+    prm.causal = causal;
+    prm.sched = schedule;
+    prm.P = P;
+    prm.scale = 1.0f / sqrtf((float)D);
+    prm.scale_log2e = prm.scale * kLog2e;
+    if (dbg && dbg->kernel_event_begin &&
+        cudaEventRecord((cudaEvent_t)dbg->kernel_event_begin, stream) != cudaSuccess)
+        return DASH_ERR_CUDA;
+    rc = launch_bwd_dispatch(D, prm, P, stream);
+    if (rc == 0 && dbg && dbg->kernel_event_end &&
+        cudaEventRecord((cudaEvent_t)dbg->kernel_event_end, stream) != cudaSuccess)
+        return DASH_ERR_CUDA;
+    if (rc == -3) return DASH_ERR_LAUNCH;
+    return rc ? DASH_ERR_CUDA : DASH_OK;
+}
+
+}  // namespace
+
+int make_tmap_2d(void* map_out, const void* base, long long rows, int D) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return -2;
+    const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+    const cuuint32_t box[2] = {64, 128};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(reinterpret_cast<CUtensorMap*>(map_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 0 : -2;
+}
+
+}  // namespace dash
+
+using namespace dash;
+
+extern "C" {
+
+int dash_attn_bwd_preprocess(const dash_bf16* o, const dash_bf16* dO, float* delta, int B, int Hq, int S, int D,
+                             dash_stream_t stream) {
+    if (!aligned16(o) || !aligned16(dO) || !aligned16(delta)) return DASH_ERR_ARG;
+    if (B <= 0 || Hq <= 0 || S <= 0 || (D != 64 && D != 128)) return DASH_ERR_ARG;
+    int dev = 0;
+    int rc = check_device(&dev);
+    if (rc) return rc;
+    return launch_preprocess(o, dO, delta, (long long)B * Hq * S, D, (cudaStream_t)stream) ? DASH_ERR_CUDA : DASH_OK;
+}
+
+int dash_attn_bwd(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const dash_bf16* o,
+                  const dash_bf16* dO, const float* lse, float* dq, dash_bf16* dk, dash_bf16* dv, int B, int Hq,
+                  int Hkv, int S, int D, int causal, int schedule, dash_stream_t stream) {
+    return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, S, D, causal, schedule, (cudaStream_t)stream,
+                    nullptr);
+}
+
+int dash_attn_bwd_debug(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const dash_bf16* o,
+                        const dash_bf16* dO, const float* lse, float* dq, dash_bf16* dk, dash_bf16* dv, int B,
+                        int Hq, int Hkv, int S, int D, int causal, int schedule, dash_stream_t stream,
+                        const dash_debug_opts* opts) {
+    return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, S, D, causal, schedule, (cudaStream_t)stream,
+                    opts);
+}
+
+int dash_dq_finalize(const float* dq_accum, dash_bf16* dq, size_t numel, dash_stream_t stream) {
+    if (!aligned16(dq_accum) || !aligned16(dq)) return DASH_ERR_ARG;
+    if (numel == 0) return DASH_OK;
+    int dev = 0;
+    int rc = check_device(&dev);
+    if (rc) return rc;
+    return launch_finalize(dq_accum, dq, numel, (cudaStream_t)stream) ? DASH_ERR_CUDA : DASH_OK;
+}
+
+int dash_get_status(dash_stream_t stream, int* code, int* info) {
+    if (!code) return DASH_ERR_ARG;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return DASH_ERR_CUDA;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DASH_ERR_CUDA;
+    Workspace* ws = get_ws(dev, (cudaStream_t)stream);
+    int h[8] = {0};
+    if (ws->ints.p && cudaMemcpy(h, ws->ints.p, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return DASH_ERR_CUDA;
+    *code = h[0];
+    if (info)
+        for (int i = 0; i < 4; ++i) info[i] = h[1 + i];
+    return DASH_OK;
+}
+
+int dash_set_timeout_ns(uint64_t ns) {
+    g_timeout_ns.store(ns ? ns : 1);
+    return DASH_OK;
+}
+
+int dash_release_workspaces(void) {
+    std::lock_guard<std::mutex> lk(g_mu);
+    int cur = 0;
+    cudaGetDevice(&cur);
+    for (auto& kv : workspaces()) {
+        cudaSetDevice(kv.first.first);
+        kv.second->release();
+        delete kv.second;
+    }
+    workspaces().clear();
+    cudaSetDevice(cur);
+    return DASH_OK;
+}
+
+int dash_num_ctas(int device, int* P) {
+    if (!P) return DASH_ERR_ARG;
+    int cur = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess) return DASH_ERR_CUDA;
+    if (cudaSetDevice(device) != cudaSuccess) return DASH_ERR_ARG;
+    int rc = bwd_max_ctas(128, device, P);
+    cudaSetDevice(cur);
+    if (rc == -3) return DASH_ERR_LAUNCH;
+    return rc ? DASH_ERR_CUDA : DASH_OK;
+}
+
+int dash_debug_tile_probe(const dash_bf16* k, const dash_bf16* v, const dash_bf16* q, const dash_bf16* dO,
+                          const float* lse, const float* delta, int D, int diag, float* sT, float* pT, float* dpT,
+                          float* dsT, float* dv, float* dk, float* dq) {
+    const void* ptrs[] = {k, v, q, dO, lse, delta, sT, pT, dpT, dsT, dv, dk, dq};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return DASH_ERR_ARG;
+    if (D != 64 && D != 128) return DASH_ERR_ARG;
+    int dev = 0;
+    int rc = check_device(&dev);
+    if (rc) return rc;
+    rc = run_tile_probe(k, v, q, dO, lse, delta, D, diag, sT, pT, dpT, dsT, dv, dk, dq);
+    if (rc == -4) return DASH_ERR_TIMEOUT;
+    if (rc == -6) return DASH_ERR_NOMEM;
+    return rc ? DASH_ERR_CUDA : DASH_OK;
+}
+
+}  // extern "C"

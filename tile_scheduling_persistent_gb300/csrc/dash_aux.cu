@@ -1,0 +1,155 @@
+// dash_aux.cu -- the small kernels around the persistent backward:
+//   preprocess  delta = rowsum(dO o O)            (memory bound)
+//   finalize    dq_bf16 = round_to_nearest_even(dq_fp32)
+//   build_ranks accumulation ranks of the static schedules (integer only)
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "dash_internal.h"
+#include "dash_schedule.h"
+
+namespace dash {
+
+namespace {
+
+// ---------------------------------------------------------------- delta
+// A group of L = D/8 lanes owns one row: each lane loads 16 B of dO and of O,
+// sums its 8 products in order, then the group reduces with a fixed
+// butterfly, so every row is summed in one fixed order.
+template <int D>
+__global__ void __launch_bounds__(256) preprocess_kernel(const uint4* __restrict__ o,
+                                                         const uint4* __restrict__ dO,
+                                                         float* __restrict__ delta, long long rows) {
+    constexpr int L = D / 8;
+    constexpr int RPW = 32 / L;   // rows per warp
+    const long long warp_global = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long row = warp_global * RPW + lane / L;
+    const int sub = lane % L;
+    float acc = 0.f;
+    if (row < rows) {
+        const uint4 a = o[row * L + sub];
+        const uint4 b = dO[row * L + sub];
+        const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+        const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 fa = __bfloat1622float2(pa[e]);
+            const float2 fb = __bfloat1622float2(pb[e]);
+            acc = fmaf(fa.x, fb.x, acc);
+            acc = fmaf(fa.y, fb.y, acc);
+        }
+    }
+#pragma unroll
+    for (int m = L / 2; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+    if (row < rows && sub == 0) delta[row] = acc;
+}
+
+// ---------------------------------------------------------------- finalize
+__global__ void __launch_bounds__(256) finalize_kernel(const float4* __restrict__ src, uint2* __restrict__ dst,
+                                                       size_t n4) {
+    for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (size_t)gridDim.x * blockDim.x) {
+        const float4 v = src[i];
+        __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+        __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+        dst[i] = make_uint2(*reinterpret_cast<uint32_t*>(&a), *reinterpret_cast<uint32_t*>(&b));
+    }
+}
+
+__global__ void finalize_tail_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst, size_t begin,
+                                     size_t end) {
+    const size_t i = begin + threadIdx.x;
+    if (i < end) dst[i] = __float2bfloat16_rn(src[i]);
+}
+
+// ---------------------------------------------------------------- ranks
+// Model time of a pair = its position in its worker's unit-step sequence
+// (worker = task % P, tasks taken in order); the accumulation rank of KV
+// tile j in dQ tile t = number of contributors of t with a smaller
+// (model time, KV index).
+__global__ void task_start_kernel(Shape s, int P, long long ntasks, uint32_t* task_start) {
+    const int w = blockIdx.x * blockDim.x + threadIdx.x;
+    if (w >= P) return;
+    uint32_t t = 0;
+    for (long long k = w; k < ntasks; k += P) {
+        task_start[k] = t;
+        t += (uint32_t)task_len(s, k);
+    }
+}
+
+__global__ void pair_time_kernel(Shape s, long long ntasks, const uint32_t* task_start, uint32_t* time) {
+    const long long k = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (k >= ntasks) return;
+    const int L = task_len(s, k);
+    const uint32_t t0 = task_start[k];
+    for (int u = 0; u < L; ++u) {
+        const Visit v = task_visit(s, k, u);
+        time[rank_index(s, v.b, v.hq, v.q, v.kv)] = t0 + (uint32_t)u;
+    }
+}
+
+__global__ void rank_kernel(int n, long long entries, const uint32_t* time, uint16_t* ranks) {
+    const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= entries) return;
+    const long long tile = e / n;
+    const int j = (int)(e % n);
+    const uint32_t* row = time + tile * n;
+    const uint32_t tj = row[j];
+    if (tj == 0xFFFFFFFFu) {
+        ranks[e] = 0xFFFF;
+        return;
+    }
+    int r = 0;
+    for (int x = 0; x < n; ++x) {
+        const uint32_t tx = row[x];
+        if (tx == 0xFFFFFFFFu) continue;
+        r += (tx < tj) || (tx == tj && x < j);
+    }
+    ranks[e] = (uint16_t)r;
+}
+
+}  // namespace
+
+int launch_preprocess(const void* o, const void* dO, float* delta, long long rows, int D, cudaStream_t s) {
+    if (rows <= 0) return 0;
+    const int L = D / 8;
+    const long long warps = (rows * L + 31) / 32;
+    const long long blocks = (warps * 32 + 255) / 256;
+    if (D == 64)
+        preprocess_kernel<64><<<(unsigned)blocks, 256, 0, s>>>((const uint4*)o, (const uint4*)dO, delta, rows);
+    else if (D == 128)
+        preprocess_kernel<128><<<(unsigned)blocks, 256, 0, s>>>((const uint4*)o, (const uint4*)dO, delta, rows);
+    else
+        return -1;
+    return cudaGetLastError() == cudaSuccess ? 0 : -2;
+}
+
+int launch_finalize(const float* src, void* dst, size_t numel, cudaStream_t s) {
+    const size_t n4 = numel / 4;
+    if (n4) {
+        int dev = 0, sms = 148;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        size_t blocks = (n4 + 255) / 256;
+        const size_t cap = (size_t)sms * 8;
+        if (blocks > cap) blocks = cap;
+        finalize_kernel<<<(unsigned)blocks, 256, 0, s>>>((const float4*)src, (uint2*)dst, n4);
+    }
+    if (numel % 4) finalize_tail_kernel<<<1, 32, 0, s>>>(src, (__nv_bfloat16*)dst, n4 * 4, numel);
+    return cudaGetLastError() == cudaSuccess ? 0 : -2;
+}
+
+int launch_build_ranks(int B, int Hq, int Hkv, int n, int causal, int sched, int P, uint16_t* ranks,
+                       uint32_t* time, uint32_t* task_start, cudaStream_t st) {
+    const Shape s{B, Hq, Hkv, n, Hq / Hkv, causal, sched};
+    const long long ntasks = num_tasks(s);
+    const long long entries = (long long)B * Hq * n * n;
+    if (cudaMemsetAsync(time, 0xFF, (size_t)entries * sizeof(uint32_t), st) != cudaSuccess) return -2;
+    task_start_kernel<<<(P + 127) / 128, 128, 0, st>>>(s, P, ntasks, task_start);
+    pair_time_kernel<<<(unsigned)((ntasks + 127) / 128), 128, 0, st>>>(s, ntasks, task_start, time);
+    rank_kernel<<<(unsigned)((entries + 255) / 256), 256, 0, st>>>(n, entries, time, ranks);
+    return cudaGetLastError() == cudaSuccess ? 0 : -2;
+}
+
+}  // namespace dash

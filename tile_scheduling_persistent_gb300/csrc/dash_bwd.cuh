@@ -1,0 +1,252 @@
+// dash_bwd.cuh -- the persistent, KV-stationary deterministic attention
+// backward kernel for sm_103a, and the tile building blocks it shares with
+// the single-tile probe.
+//
+// One CTA per SM.  A CTA takes tasks (one KV tile, or a symmetric pair of KV
+// tiles) either from a static round-robin assignment (shift, symmetric shift)
+// or from a global counter in task order (the other schedules).  For each
+// pair (KV tile j, Q tile i) of a task:
+//
+//   S^T  = K_j Q_i^T            (tcgen05, both operands K-major in smem)
+//   P^T  = exp(scale S^T - LSE_i)      (masked on the causal diagonal)
+//   dV_j += P^T dO_i            (A = P^T from tensor memory, packed bf16)
+//   dP^T = V_j dO_i^T
+//   dS^T = scale * P^T o (dP^T - delta_i)   (bf16, smem)
+//   dK_j += dS^T Q_i            (B = Q MN-major)
+//   dQ_i^(j) = dS K_j           (A = dS^T read MN-major, B = K MN-major)
+//   dq[tile i] += dQ_i^(j)      (fp32, after waiting for this pair's turn)
+//
+// The ordered reduction is the one the DASH pages describe: a per-dQ-tile
+// counter (the release side is the "safe_signal" counter of the pwwt.cn
+// write-up, section 3.1), each contributor waiting until the counter equals
+// its rank in the schedule's accumulation order (gist.science DASH summary,
+// section 1: a fixed accumulation order makes dQ reproducible).
+//
+// Warp roles (16 warps, 512 threads):
+//   warps 0-3   reducer: drain dQ from TMEM, ordered fp32 reduction into
+//               global dq, and the dK/dV epilogue of each KV tile;
+//   warp 4      producer: task dispatch, pair descriptors, TMA loads;
+//   warp 5      MMA issuer (one thread) and TMEM owner;
+//   warps 6-7   idle;
+//   warps 8-15  softmax / dS: warp w owns TMEM lanes 32*(w%4).. and the Q
+//               columns 64*((w-8)/4) .. +63 of the pair.
+//
+// Tensor memory (512 columns): dK [0,D), dV [D,2D), S/P [2D, 2D+128),
+// dP [2D+128, 2D+256); dQ aliases dP when D = 128 and has its own 64
+// columns when D = 64.
+//
+// Every wait is bounded (%globaltimer); a wait that runs out records the
+// failure in the status word, raises a CTA-wide and a grid-wide abort flag,
+// and every role then leaves its loop; the CTA waits for its own TMA loads
+// and MMAs to land, frees tensor memory and exits.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "dash_ptx.cuh"
+#include "dash_schedule.h"
+
+namespace dash {
+
+constexpr int kThreads = 512;
+constexpr int kBox = 16384;        // 128 rows x 128 B
+constexpr int kNDesc = 8;          // pair-descriptor ring depth
+constexpr int kStages = 2;         // Q/dO/LSE/delta stages
+constexpr float kLog2e = 1.4426950408889634f;
+
+enum Role : int { kRoleReducer = 0, kRoleProducer = 1, kRoleMma = 2, kRoleSoftmax = 3 };
+enum DescFlags : int { kKvFirst = 1, kKvLast = 2, kDiag = 4, kEnd = 8 };
+
+// Barrier slots (8 bytes each) at the start of the control area.
+enum Bar : int {
+    B_DESC_FULL = 0,
+    B_DESC_EMPTY = B_DESC_FULL + kNDesc,
+    B_KV_FULL = B_DESC_EMPTY + kNDesc,
+    B_KV_EMPTY,
+    B_Q_FULL,
+    B_Q_EMPTY = B_Q_FULL + kStages,
+    B_S_FULL = B_Q_EMPTY + kStages,
+    B_DP_FULL,
+    B_P_READY,
+    B_DS_READY,
+    B_DS_FREE,
+    B_DQ_FULL,
+    B_DQ_EMPTY,
+    B_ACC_FULL,
+    B_ACC_EMPTY,
+    B_DRAIN,
+    B_COUNT
+};
+
+static_assert(B_COUNT * 8 <= 256, "barrier area");
+
+struct PairDesc {
+    int b, hq, hkv, q, kv, flags, rank, pad;
+};
+static_assert(sizeof(PairDesc) * kNDesc <= 256, "descriptor ring area");
+
+template <int D>
+struct Cfg {
+    static constexpr int kTile = D * 128 * 2;         // 128 x D bf16
+    static constexpr int kNBox = D / 64;
+    static constexpr int OFF_K = 0;
+    static constexpr int OFF_V = OFF_K + kTile;
+    static constexpr int OFF_STAGE = OFF_V + kTile;    // stage s: Q at +2s*kTile, dO at +(2s+1)*kTile
+    static constexpr int OFF_DS = OFF_STAGE + kStages * 2 * kTile;
+    static constexpr int OFF_VEC = OFF_DS + 2 * kBox;  // per stage: LSE[128], delta[128]
+    static constexpr int OFF_CTL = OFF_VEC + kStages * 1024;
+    static constexpr int CTL_BYTES = 1024;             // barriers, descriptors, flags
+    static constexpr int kSmem = OFF_CTL + CTL_BYTES;
+    static constexpr uint32_t COL_DK = 0;
+    static constexpr uint32_t COL_DV = D;
+    static constexpr uint32_t COL_S = 2 * D;
+    static constexpr uint32_t COL_DP = 2 * D + 128;
+    static constexpr bool kDqAlias = (D == 128);
+    static constexpr uint32_t COL_DQ = kDqAlias ? COL_DP : 2 * D + 256;
+    static constexpr uint32_t kStageBytes = 2 * kTile + 1024;
+    static constexpr uint32_t kKvBytes = 2 * kTile;
+    static_assert(kSmem <= 232448, "shared memory budget");
+    static_assert(COL_DQ + D <= 512, "tensor memory budget");
+};
+
+struct BwdParams {
+    CUtensorMap tm_q, tm_k, tm_v, tm_do;   // 2D [rows, D] bf16, box 64 x 128, SWIZZLE_128B
+    const float* lse;
+    const float* delta;
+    float* dq;
+    __nv_bfloat16* dk;
+    __nv_bfloat16* dv;
+    const uint16_t* ranks;                  // static schedules: [B*Hq*n][n]
+    int* sem;                               // [B*Hq*n] accumulation counters
+    int* logcnt;                            // [B*Hq*n] order-log cursors
+    int* task_counter;                      // dynamic dispatch
+    int* status;                            // [8]: code, info[4]
+    int* abort_flag;                        // grid-wide abort
+    int32_t* order_log;                     // debug, may be null
+    float* partials;                        // debug, may be null
+    const int32_t* cta_perm;                // debug, may be null
+    const int64_t* delay_ns;                // debug, may be null
+    unsigned long long timeout_ns;
+    long long ntasks;
+    int B, Hq, Hkv, S, n, G, causal, sched, P;
+    float scale, scale_log2e;
+};
+
+// ------------------------------------------------------------------ MMA issue
+// All operand addresses are shared-window byte addresses of 1024-aligned
+// 128-row boxes.
+
+template <int D>
+__device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t sA, uint32_t sB) {
+    // [128 x 128] = A[128 x D] * B[128 x D]^T, both K-major
+    constexpr uint32_t idesc = ptx::idesc_bf16(128, 128, 0, 0);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+        ptx::mma_ss(d_tmem, ptx::sdesc(sA + off, 16, 1024), ptx::sdesc(sB + off, 16, 1024), idesc,
+                    kk > 0);
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_dv(uint32_t d_tmem, uint32_t p_tmem, uint32_t sDo,
+                                         uint32_t acc) {
+    // dV[128 x D] (+)= P^T[128 x 128] (tmem, K-major) * dO[128 x D] (MN-major)
+    constexpr uint32_t idesc = ptx::idesc_bf16(128, D, 0, 1);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t a = p_tmem + (kk >> 2) * 64 + (kk & 3) * 8;
+        ptx::mma_ts(d_tmem, a, ptx::sdesc(sDo + kk * 2048, kBox, 1024), idesc, acc | (kk > 0));
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_dk(uint32_t d_tmem, uint32_t sDsT, uint32_t sQ, uint32_t acc) {
+    // dK[128 x D] (+)= dS^T[128 x 128] (K-major) * Q[128 x D] (MN-major)
+    constexpr uint32_t idesc = ptx::idesc_bf16(128, D, 0, 1);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
+        ptx::mma_ss(d_tmem, ptx::sdesc(sDsT + aoff, 16, 1024), ptx::sdesc(sQ + kk * 2048, kBox, 1024),
+                    idesc, acc | (kk > 0));
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void issue_dq(uint32_t d_tmem, uint32_t sDsT, uint32_t sK) {
+    // dQ[128 x D] = dS[128 x 128] (dS^T read MN-major) * K[128 x D] (MN-major)
+    constexpr uint32_t idesc = ptx::idesc_bf16(128, D, 1, 1);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        ptx::mma_ss(d_tmem, ptx::sdesc(sDsT + kk * 2048, kBox, 1024),
+                    ptx::sdesc(sK + kk * 2048, kBox, 1024), idesc, kk > 0);
+    }
+}
+
+// ------------------------------------------------------------ softmax / dS
+// Executed by one warp that owns TMEM lanes [lane_base, lane_base+32) (KV rows)
+// and Q columns [c0, c0+64) of the pair.
+
+// P for 64 columns: reads S^T, writes P (fp32, registers) and the packed
+// bf16 P^T back into tensor memory at columns [col_s + c0/2 .. ) of its own
+// 64-column span (so the MMA reads it as a K-major A operand).
+__device__ __forceinline__ void softmax_64(uint32_t tmem_s_lane, int c0, const float* lse,
+                                           float scale_log2e, bool diag, int row, float (&P)[64]) {
+    uint32_t r0[32], r1[32];
+    ptx::tmem_ld32(tmem_s_lane + c0, r0);
+    ptx::tmem_ld32(tmem_s_lane + c0 + 32, r1);
+    ptx::tmem_ld_wait();
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        const int q = c0 + k;
+        float x = ptx::ex2(fmaf(__uint_as_float(r0[k]), scale_log2e, -lse[q] * kLog2e));
+        P[k] = (diag && row > q) ? 0.f : x;
+    }
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        const int q = c0 + 32 + k;
+        float x = ptx::ex2(fmaf(__uint_as_float(r1[k]), scale_log2e, -lse[q] * kLog2e));
+        P[32 + k] = (diag && row > q) ? 0.f : x;
+    }
+    uint32_t pk[32];
+#pragma unroll
+    for (int k = 0; k < 32; ++k) {
+        __nv_bfloat162 h2 = __floats2bfloat162_rn(P[2 * k], P[2 * k + 1]);
+        pk[k] = *reinterpret_cast<uint32_t*>(&h2);
+    }
+    ptx::tmem_st32(tmem_s_lane + c0, pk);
+    ptx::tmem_st_wait();
+}
+
+// dS^T = scale * P o (dP^T - delta) for 64 columns; the bf16 result goes to
+// the K-major swizzled box `box_saddr` (row `row`), i.e. box c0/64 of dS^T.
+__device__ __forceinline__ void ds_64(uint32_t tmem_dp_lane, int c0, const float* delta, float scale,
+                                      const float (&P)[64], uint32_t pk[32]) {
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        uint32_t r[32];
+        ptx::tmem_ld32(tmem_dp_lane + c0 + 32 * half, r);
+        ptx::tmem_ld_wait();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int a = 32 * half + 2 * k;
+            const float d0 = P[a] * (__uint_as_float(r[2 * k]) - delta[c0 + a]) * scale;
+            const float d1 = P[a + 1] * (__uint_as_float(r[2 * k + 1]) - delta[c0 + a + 1]) * scale;
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(d0, d1);
+            pk[16 * half + k] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+    }
+}
+
+__device__ __forceinline__ void store_row_sw128(uint8_t* box, int row, const uint32_t pk[32]) {
+    // 64 bf16 = 8 chunks of 16 B; chunk c lands at (c ^ (row % 8)) in the row.
+    uint8_t* rp = box + row * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        *reinterpret_cast<uint4*>(rp + ((c ^ (row & 7)) << 4)) = v;
+    }
+}
+
+}  // namespace dash

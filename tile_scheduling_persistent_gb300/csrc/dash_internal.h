@@ -1,0 +1,32 @@
+// dash_internal.h -- declarations shared by the translation units of libdash.
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dash {
+
+struct BwdParams;
+
+// Persistent backward kernel (dash_bwd.cu).
+int launch_bwd_dispatch(int D, const BwdParams& prm, int grid, cudaStream_t stream);
+int bwd_max_ctas(int D, int device, int* P);
+int bwd_smem_bytes(int D);
+
+// Auxiliary kernels (dash_aux.cu).
+int launch_preprocess(const void* o, const void* dO, float* delta, long long rows, int D, cudaStream_t s);
+int launch_finalize(const float* src, void* dst, size_t numel, cudaStream_t s);
+// Accumulation ranks of a static schedule, built on the device:
+// ranks [B*Hq*n][n] (uint16), scratch `time` [B*Hq*n][n] (uint32),
+// `task_start` [num_tasks] (uint32).
+int launch_build_ranks(int B, int Hq, int Hkv, int n, int causal, int sched, int P, uint16_t* ranks,
+                       uint32_t* time, uint32_t* task_start, cudaStream_t s);
+
+// Single-tile probe (dash_probe.cu).
+int run_tile_probe(const void* k, const void* v, const void* q, const void* dO, const float* lse,
+                   const float* delta, int D, int diag, float* sT, float* pT, float* dpT, float* dsT,
+                   float* dv, float* dk, float* dq);
+
+// Tensor maps (dash_api.cu).
+int make_tmap_2d(void* map_out, const void* base, long long rows, int D);
+
+}  // namespace dash

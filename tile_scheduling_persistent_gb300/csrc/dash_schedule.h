@@ -1,0 +1,125 @@
+// dash_schedule.h -- the tile schedules of DASH as closed-form functions.
+//
+// Shared by the persistent kernel (the producer warp walks a task's visit
+// list), the device table builder and the host simulator.  Definitions
+// follow "DASH: Deterministic Attention Scheduling for High-Throughput"
+// (gist.science technical summary), section 2.2:
+//   - descending Q-tile iteration (2.2.A): Q tiles visited n-1 .. 0;
+//   - shift scheduling (2.2.B, full masks): the worker that owns KV tile j
+//     visits Q tiles j, j+1, ..., n-1, 0, ..., j-1 (the summary words it as
+//     "SM i processes i, i+1, ..., N-1, 0, ..., i-1"; with the KV tile kept
+//     resident it is the Q tiles that rotate);
+//   - symmetric shift (2.2.B, causal masks): KV tiles jp and n-1-jp form one
+//     task; phase 1 is the dense rectangle (KV jp against the last h = n/2 Q
+//     tiles, rotated by jp), phase 2 the folded triangle (KV jp against Q
+//     jp .. n-h-1 ascending, then KV n-1-jp against Q n-1 .. n-1-jp).
+// and the FlashAttention-3-style baseline (ascending visits, ascending-KV
+// accumulation order) that the summary's section 1 describes.
+//
+// A task is one KV tile (b, hkv, j) -- or one symmetric pair -- and runs the
+// pairs of every query head of its group (ascending) back to back on one
+// CTA, so dK/dV stay in tensor memory for the whole task.
+#pragma once
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define DASH_HD __host__ __device__ __forceinline__
+#else
+#define DASH_HD inline
+#endif
+
+namespace dash {
+
+enum Sched : int {
+    kAtomic = 0,
+    kAscending = 1,
+    kDescending = 2,
+    kShift = 3,
+    kSymmetric = 4,
+};
+
+struct Shape {
+    int B, Hq, Hkv, n, G, causal, sched;
+};
+
+// Symmetric shift only exists on causal masks; on a full mask it is shift.
+DASH_HD bool is_symmetric(const Shape& s) { return s.sched == kSymmetric && s.causal; }
+DASH_HD bool is_static(int sched) { return sched == kShift || sched == kSymmetric; }
+DASH_HD bool is_ordered(int sched) { return sched != kAtomic; }
+
+// Tasks per (b, hkv) and in total.
+DASH_HD int tasks_per_group(const Shape& s) { return is_symmetric(s) ? (s.n + 1) / 2 : s.n; }
+DASH_HD int64_t num_tasks(const Shape& s) {
+    return (int64_t)s.B * s.Hkv * tasks_per_group(s);
+}
+
+// Visits of one KV tile j for ONE query head (non-symmetric schedules).
+DASH_HD int kv_len(const Shape& s, int j) { return s.causal ? s.n - j : s.n; }
+
+// Pairs in task k (all heads of the group).
+DASH_HD int task_len(const Shape& s, int64_t k) {
+    int t = (int)(k % tasks_per_group(s));
+    if (!is_symmetric(s)) return s.G * kv_len(s, t);
+    const int h = s.n / 2;
+    if ((s.n & 1) && t == h) return s.G * (s.n - h);   // middle tile of an odd n
+    return s.G * (s.n + 1);
+}
+
+struct Visit {
+    int b, hkv, hq, kv, q;   // dQ tile (b, hq, q) receives the partial of KV tile (b, hkv, kv)
+};
+
+// The u-th pair of task k, 0 <= u < task_len(s, k).
+DASH_HD Visit task_visit(const Shape& s, int64_t k, int u) {
+    const int T = tasks_per_group(s);
+    Visit v;
+    const int t = (int)(k % T);
+    const int64_t bh = k / T;
+    v.hkv = (int)(bh % s.Hkv);
+    v.b = (int)(bh / s.Hkv);
+    const int n = s.n;
+    if (!is_symmetric(s)) {
+        const int j = t;
+        const int L = kv_len(s, j);
+        const int g = u / L, w = u % L;
+        v.hq = v.hkv * s.G + g;
+        v.kv = j;
+        switch (s.sched) {
+            case kDescending: v.q = n - 1 - w; break;
+            case kShift:
+            case kSymmetric:  v.q = s.causal ? j + w : (j + w) % n; break;   // symmetric on a full mask = shift
+            default:          v.q = (s.causal ? j : 0) + w; break;   // ascending, atomic
+        }
+        return v;
+    }
+    const int h = n / 2;
+    const int jp = t;
+    if ((n & 1) && jp == h) {                   // middle tile: descending visits
+        const int L = n - h;
+        v.hq = v.hkv * s.G + u / L;
+        v.kv = h;
+        v.q = n - 1 - (u % L);
+        return v;
+    }
+    const int La = n - jp;                      // phase 1 (h) + phase 2a (n-h-jp)
+    if (u < s.G * La) {
+        const int g = u / La, w = u % La;
+        v.hq = v.hkv * s.G + g;
+        v.kv = jp;
+        v.q = (w < h) ? (n - h) + (jp + w) % h : jp + (w - h);
+        return v;
+    }
+    const int ub = u - s.G * La;                // phase 2b: KV n-1-jp, descending Q
+    const int Lb = jp + 1;
+    v.hq = v.hkv * s.G + ub / Lb;
+    v.kv = n - 1 - jp;
+    v.q = n - 1 - (ub % Lb);
+    return v;
+}
+
+// Index of the accumulation-rank entry of pair (b, hq, q, kv).
+DASH_HD int64_t rank_index(const Shape& s, int b, int hq, int q, int kv) {
+    return (((int64_t)b * s.Hq + hq) * s.n + q) * s.n + kv;
+}
+
+}  // namespace dash

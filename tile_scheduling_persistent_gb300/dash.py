@@ -1,0 +1,199 @@
+"""ctypes binding of libdash.so (C ABI in include/dash.h).
+
+Argument marshalling only: every step of the backward pass runs in the
+library's CUDA kernels.  Tensors are torch CUDA tensors (device memory and
+streams come from PyTorch); the library fails loudly if it is missing.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+from .inputs import SCHEDULE_IDS
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libdash.so")
+
+OK, ERR_ARG, ERR_CUDA, ERR_LAUNCH, ERR_TIMEOUT, ERR_DEADLOCK, ERR_NOMEM, ERR_DEVICE = 0, -1, -2, -3, -4, -5, -6, -7
+_NAMES = {0: "DASH_OK", -1: "DASH_ERR_ARG", -2: "DASH_ERR_CUDA", -3: "DASH_ERR_LAUNCH", -4: "DASH_ERR_TIMEOUT",
+          -5: "DASH_ERR_DEADLOCK", -6: "DASH_ERR_NOMEM", -7: "DASH_ERR_DEVICE"}
+
+EXPORTS = (
+    "dash_attn_bwd_preprocess", "dash_attn_bwd", "dash_dq_finalize", "dash_get_status", "dash_set_timeout_ns",
+    "dash_release_workspaces", "dash_num_ctas", "dash_sim_schedule", "dash_sim_check_ranks",
+    "dash_attn_bwd_debug", "dash_debug_tile_probe",
+)
+
+
+class DashError(RuntimeError):
+    def __init__(self, code, what):
+        super().__init__("%s failed: %s (%d)" % (what, _NAMES.get(code, "?"), code))
+        self.code = code
+
+
+class _DebugOpts(ctypes.Structure):
+    _fields_ = [("order_log", ctypes.c_void_p), ("dq_partials", ctypes.c_void_p), ("cta_perm", ctypes.c_void_p),
+                ("start_delay_ns", ctypes.c_void_p), ("ranks_host", ctypes.c_void_p),
+                ("skip_table_check", ctypes.c_int), ("kernel_event_begin", ctypes.c_void_p),
+                ("kernel_event_end", ctypes.c_void_p)]
+
+
+_lib = None
+
+
+def lib():
+    """Load libdash.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError("libdash.so is not built (run: python -m tile_scheduling_persistent_gb300.build)")
+    L = ctypes.CDLL(LIB_PATH)
+    P, I, Z, D = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_double
+    L.dash_attn_bwd_preprocess.argtypes = [P, P, P, I, I, I, I, P]
+    L.dash_attn_bwd.argtypes = [P] * 9 + [I] * 7 + [P]
+    L.dash_attn_bwd_debug.argtypes = [P] * 9 + [I] * 7 + [P, ctypes.POINTER(_DebugOpts)]
+    L.dash_dq_finalize.argtypes = [P, P, Z, P]
+    L.dash_get_status.argtypes = [P, ctypes.POINTER(I), ctypes.POINTER(I)]
+    L.dash_set_timeout_ns.argtypes = [ctypes.c_uint64]
+    L.dash_release_workspaces.argtypes = []
+    L.dash_num_ctas.argtypes = [I, ctypes.POINTER(I)]
+    L.dash_sim_schedule.argtypes = [I] * 7 + [D, D, ctypes.POINTER(D), P, ctypes.POINTER(ctypes.c_int64)]
+    L.dash_sim_check_ranks.argtypes = [I] * 7 + [P]
+    L.dash_debug_tile_probe.argtypes = [P] * 6 + [I, I] + [P] * 7
+    for name in EXPORTS:
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def _check(rc, what):
+    if rc != OK:
+        raise DashError(rc, what)
+
+
+def _sched(schedule):
+    return SCHEDULE_IDS[schedule] if isinstance(schedule, str) else int(schedule)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t, dtype=None):
+    if t is None:
+        return None
+    assert t.is_cuda and t.is_contiguous(), "expected a contiguous CUDA tensor"
+    if dtype is not None:
+        assert t.dtype == dtype, "expected %s, got %s" % (dtype, t.dtype)
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def attn_bwd_preprocess(o, do, delta, stream=None):
+    B, H, S, D = o.shape
+    _check(lib().dash_attn_bwd_preprocess(_ptr(o, torch.bfloat16), _ptr(do, torch.bfloat16),
+                                          _ptr(delta, torch.float32), B, H, S, D, _stream(stream)),
+           "dash_attn_bwd_preprocess")
+
+
+def _bwd_args(q, k, v, o, do, lse, dq, dk, dv, causal, schedule):
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    bf, f32 = torch.bfloat16, torch.float32
+    return [_ptr(q, bf), _ptr(k, bf), _ptr(v, bf), _ptr(o, bf), _ptr(do, bf), _ptr(lse, f32), _ptr(dq, f32),
+            _ptr(dk, bf), _ptr(dv, bf), B, Hq, Hkv, S, D, int(bool(causal)), _sched(schedule)]
+
+
+def attn_bwd(q, k, v, o, do, lse, dq, dk, dv, causal, schedule, stream=None):
+    """dq (fp32 accumulator, zeroed by the library), dk, dv (bf16) <- backward."""
+    _check(lib().dash_attn_bwd(*_bwd_args(q, k, v, o, do, lse, dq, dk, dv, causal, schedule), _stream(stream)),
+           "dash_attn_bwd")
+
+
+def attn_bwd_debug(q, k, v, o, do, lse, dq, dk, dv, causal, schedule, stream=None, order_log=None,
+                   dq_partials=None, cta_perm=None, start_delay_ns=None, ranks_host=None, skip_table_check=False,
+                   kernel_events=None):
+    opts = _DebugOpts()
+    if kernel_events is not None:
+        opts.kernel_event_begin = ctypes.c_void_p(kernel_events[0].cuda_event)
+        opts.kernel_event_end = ctypes.c_void_p(kernel_events[1].cuda_event)
+    opts.order_log = _ptr(order_log, torch.int32)
+    opts.dq_partials = _ptr(dq_partials, torch.float32)
+    opts.cta_perm = _ptr(cta_perm, torch.int32)
+    opts.start_delay_ns = _ptr(start_delay_ns, torch.int64)
+    keep = None
+    if ranks_host is not None:
+        keep = np.ascontiguousarray(ranks_host, dtype=np.uint16)
+        opts.ranks_host = keep.ctypes.data_as(ctypes.c_void_p)
+    opts.skip_table_check = int(bool(skip_table_check))
+    rc = lib().dash_attn_bwd_debug(*_bwd_args(q, k, v, o, do, lse, dq, dk, dv, causal, schedule),
+                                   _stream(stream), ctypes.byref(opts))
+    if keep is not None:
+        torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
+    _check(rc, "dash_attn_bwd_debug")
+
+
+def dq_finalize(dq_accum, dq, stream=None):
+    assert dq_accum.numel() == dq.numel()
+    _check(lib().dash_dq_finalize(_ptr(dq_accum, torch.float32), _ptr(dq, torch.bfloat16), dq.numel(),
+                                  _stream(stream)), "dash_dq_finalize")
+
+
+def get_status(stream=None):
+    code = ctypes.c_int(0)
+    info = (ctypes.c_int * 4)()
+    _check(lib().dash_get_status(_stream(stream), ctypes.byref(code), info), "dash_get_status")
+    return code.value, list(info)
+
+
+def set_timeout_ns(ns):
+    _check(lib().dash_set_timeout_ns(int(ns)), "dash_set_timeout_ns")
+
+
+def release_workspaces():
+    _check(lib().dash_release_workspaces(), "dash_release_workspaces")
+
+
+def num_ctas(device=None):
+    dev = torch.cuda.current_device() if device is None else int(device)
+    P = ctypes.c_int(0)
+    _check(lib().dash_num_ctas(dev, ctypes.byref(P)), "dash_num_ctas")
+    return P.value
+
+
+def sim_schedule(schedule, causal, B, Hq, Hkv, n, P, c=1.0, r=1.0, turn_order=True):
+    """Host DAG simulator: (makespan, turn order [B*Hq*n, n] or None, tasks)."""
+    mk = ctypes.c_double(0.0)
+    nt = ctypes.c_int64(0)
+    out = np.empty((B * Hq * n, n), dtype=np.int32) if turn_order else None
+    rc = lib().dash_sim_schedule(_sched(schedule), int(bool(causal)), B, Hq, Hkv, n, P, float(c), float(r),
+                                 ctypes.byref(mk), out.ctypes.data_as(ctypes.c_void_p) if out is not None else None,
+                                 ctypes.byref(nt))
+    _check(rc, "dash_sim_schedule")
+    return mk.value, out, nt.value
+
+
+def sim_check_ranks(schedule, causal, B, Hq, Hkv, n, P, ranks):
+    arr = np.ascontiguousarray(ranks, dtype=np.uint16)
+    return lib().dash_sim_check_ranks(_sched(schedule), int(bool(causal)), B, Hq, Hkv, n, P,
+                                      arr.ctypes.data_as(ctypes.c_void_p))
+
+
+def tile_probe(k, v, q, do, lse, delta, diag=False):
+    """One pair through the kernel's building blocks; returns fp32 intermediates."""
+    D = k.shape[-1]
+    dev = k.device
+    f = lambda *s: torch.empty(*s, dtype=torch.float32, device=dev)  # noqa: E731
+    out = {name: f(128, 128) for name in ("sT", "pT", "dpT", "dsT")}
+    out.update({name: f(128, D) for name in ("dv", "dk", "dq")})
+    bf = torch.bfloat16
+    _check(lib().dash_debug_tile_probe(_ptr(k, bf), _ptr(v, bf), _ptr(q, bf), _ptr(do, bf),
+                                       _ptr(lse, torch.float32), _ptr(delta, torch.float32), D, int(bool(diag)),
+                                       *[_ptr(out[n]) for n in ("sT", "pT", "dpT", "dsT", "dv", "dk", "dq")]),
+           "dash_debug_tile_probe")
+    return out
