@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--impl", default="dash", choices=["dash", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--kernel-only", action="store_true",
+                    help="only W + K steps of --schedule (for profiler captures); prints a short JSON line")
     return ap.parse_args()
 
 
@@ -160,6 +162,8 @@ def time_schedule(w, sched, tensors, outs, steps, warmup, stream, kernel_events=
     def step(i):
         if kernel_events:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)   # torch creates events lazily: make both handles exist;
+            e1.record(stream)   # the library re-records them around the kernel launch
             dash.attn_bwd_debug(q, k, v, o, do, lse, dq, dk, dv, w.causal, sched, stream=stream,
                                 kernel_events=(e0, e1))
             evs.append((e0, e1))
@@ -214,12 +218,20 @@ def main_gpu(args):
     if args.schedule:
         det = [args.schedule]
 
+    if args.kernel_only:
+        sched = args.schedule or det[0]
+        ms, _, lps = time_schedule(w, sched, tensors, outs, args.steps, args.warmup, stream)
+        print(json.dumps({"workload": w.name, "schedule": sched, "ms_per_step": round(ms, 4),
+                          "tflops": round(flop / (ms * 1e-3) / 1e12, 2), "gpu_launches": lps * args.steps}))
+        return
+
     # pick the best deterministic schedule on a short untimed probe run
     trial = {}
     for s in det:
         ms, _, _ = time_schedule(w, s, tensors, outs, 3, 2, stream)
         trial[s] = ms
     best = min(trial, key=trial.get)
+    print("schedule trials (ms/step): %s" % trial, file=sys.stderr, flush=True)
 
     def barrier():
         if dist is not None:

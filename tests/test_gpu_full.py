@@ -1,0 +1,117 @@
+"""Full-size workloads: sampled parity with the fp64 oracle, bitwise
+reproducibility, order logs vs the simulator, and whole-tensor properties.
+
+At these sizes the oracle cannot produce whole tensors in seconds, so it is
+run exactly (fp64 forward for O and LSE, then the backward one row at a time)
+on sampled key/value head groups and sampled rows; the kernel is launched in
+the same configuration the benchmark times.  Heads outside the sampled
+groups get O and LSE from a plain fp32 PyTorch forward on the GPU (input
+synthesis only).  Whole tensors are checked by properties that hold at any
+size: finiteness, agreement with the unordered-atomics result of the same
+kernel, and determinism.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as A
+from tile_scheduling_persistent_gb300 import dash
+from tile_scheduling_persistent_gb300.inputs import WORKLOADS, make_workload_inputs
+
+from gpu_helpers import MAX_ABS, REL_L2, err, gpu_forward_fp32, same_bits, sim_turns, Case
+
+pytestmark = pytest.mark.gpu
+
+FULL = [w for w in WORKLOADS if w != "full_b1_h2_s512_d64"]
+_cache = {}
+
+
+def sampled_groups(w):
+    G = w.Hq // w.Hkv
+    if G > 1:
+        return [(0, 0)]
+    return [(0, 0), (w.B - 1, w.Hkv - 1)]
+
+
+def sample_rows(S, seed):
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, 127, 128, S // 2, S - 129, S - 128, S - 1]
+    return sorted(set(fixed + list(rng.integers(0, S, 4))))
+
+
+def setup(name):
+    if name in _cache:
+        return _cache[name]
+    w = WORKLOADS[name]
+    q, k, v, do = make_workload_inputs(w, seed=0)
+    dev = torch.device("cuda")
+    qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
+    o, lse = gpu_forward_fp32(qd, kd, vd, w.causal)
+    G = w.Hq // w.Hkv
+    exact = {}
+    workers = min(8, len(os.sched_getaffinity(0)))
+    for (b, hk) in sampled_groups(w):
+        heads = list(range(hk * G, (hk + 1) * G))
+        qs, ks, vs = q[b:b + 1, heads], k[b:b + 1, hk:hk + 1], v[b:b + 1, hk:hk + 1]
+        o_ex, lse_ex = A.attn_fwd(qs, ks, vs, w.causal, row_block=2048, workers=workers)
+        exact[(b, hk)] = (o_ex, lse_ex)
+        o[b, heads] = torch.from_numpy(o_ex[0]).to(torch.bfloat16).to(dev)
+        lse[b, heads] = torch.from_numpy(lse_ex[0]).to(torch.float32).to(dev)
+    c = Case(w.B, w.Hq, w.Hkv, w.S, w.D, w.causal, qd, kd, vd, o, dod, lse, None)
+    _cache[name] = (w, c, (q, k, v, do), exact)
+    return _cache[name]
+
+
+def run_full(c, sched, **dbg):
+    dq = torch.empty(c.B, c.Hq, c.S, c.D, dtype=torch.float32, device="cuda")
+    dk = torch.empty(c.B, c.Hkv, c.S, c.D, dtype=torch.bfloat16, device="cuda")
+    dv = torch.empty_like(dk)
+    if dbg:
+        dash.attn_bwd_debug(c.q, c.k, c.v, c.o, c.do, c.lse, dq, dk, dv, c.causal, sched, **dbg)
+    else:
+        dash.attn_bwd(c.q, c.k, c.v, c.o, c.do, c.lse, dq, dk, dv, c.causal, sched)
+    dqb = torch.empty(dq.shape, dtype=torch.bfloat16, device="cuda")
+    dash.dq_finalize(dq, dqb)
+    code, info = dash.get_status()
+    assert code == 0, (code, info)
+    return dq, dqb, dk, dv
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size(name):
+    w, c, host, exact = setup(name)
+    q, k, v, do = host
+    G = w.Hq // w.Hkv
+    nd = run_full(c, "atomic_nondet")
+    for sched in w.schedules:
+        if sched == "atomic_nondet":
+            got = nd
+        else:
+            log = torch.full((c.B * c.Hq * c.n, c.n), -1, dtype=torch.int32, device="cuda")
+            got = run_full(c, sched, order_log=log)
+            again = run_full(c, sched)
+            for a, b in zip(got, again):
+                assert same_bits(a, b), sched
+            np.testing.assert_array_equal(log.cpu().numpy(), sim_turns(c, sched))
+        dq, dqb, dk, dv = got
+        for t in got:
+            assert torch.isfinite(t.float()).all()
+        # whole tensors: the ordered result agrees with the unordered one
+        for a, b in ((dq, nd[0]), (dk, nd[2]), (dv, nd[3])):
+            a, b = a.float(), b.float()
+            assert float((a - b).norm() / b.norm()) < 2e-3, sched
+        # sampled rows against the exact fp64 oracle
+        for (b, hk), (o_ex, lse_ex) in exact.items():
+            heads = list(range(hk * G, (hk + 1) * G))
+            qs, ks, vs, dos = q[b:b + 1, heads], k[b:b + 1, hk:hk + 1], v[b:b + 1, hk:hk + 1], do[b:b + 1, heads]
+            rows = sample_rows(w.S, seed=b * 1000 + hk)
+            for gi, hq in enumerate(heads):
+                ref = A.dq_rows(qs, ks, vs, o_ex, dos, lse_ex, w.causal, 0, gi, rows)
+                rel, mx = err(dqb[b, hq, rows], ref)
+                assert rel <= REL_L2 and mx <= MAX_ABS, (sched, "dq", b, hq, rel, mx)
+            rk, rv = A.dkv_rows(qs, ks, vs, o_ex, dos, lse_ex, w.causal, 0, 0, rows)
+            for nm, g, ref in (("dk", dk[b, hk, rows], rk), ("dv", dv[b, hk, rows], rv)):
+                rel, mx = err(g, ref)
+                assert rel <= REL_L2 and mx <= MAX_ABS, (sched, nm, b, hk, rel, mx)

@@ -46,21 +46,18 @@ __device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, const Ctl& 
     return true;
 }
 
-// Whole-warp bounded wait with a warp-uniform outcome.
+// Whole-warp bounded wait with a warp-uniform outcome: lane 0 polls, then
+// every lane observes the completed phase itself (acquire per thread).
 __device__ __forceinline__ bool waitw(uint32_t bar, uint32_t parity, const Ctl& c, int role, int i0,
                                       int i1) {
-    bool done = ptx::mbar_try_wait(bar, parity);
-    if (__all_sync(0xffffffffu, done)) return true;
-    const uint64_t t0 = ptx::globaltimer();
-    for (;;) {
-        if (!done) done = ptx::mbar_try_wait(bar, parity);
-        if (__all_sync(0xffffffffu, done)) return true;
-        const bool bail = (*c.abort_smem != 0) || (ptx::globaltimer() - t0 > c.timeout);
-        if (__any_sync(0xffffffffu, bail)) {
-            if ((threadIdx.x & 31) == 0 && *c.abort_smem == 0) report_timeout(c, role, i0, i1, (int)bar);
-            return false;
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = wait1(bar, parity, c, role, i0, i1) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok) {
+        while (!ptx::mbar_try_wait(bar, parity)) {
         }
     }
+    return ok != 0;
 }
 
 // Barrier among the 4 reducer warps that also ORs a predicate.
@@ -415,22 +412,37 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
             float* gpart = p.partials
                                ? p.partials + (((size_t)tile * p.n + d.kv) * 128 + row) * D
                                : nullptr;
-#pragma unroll
-            for (int cc = 0; cc < D / 32; ++cc) {
-                uint32_t r[32];
-                ptx::tmem_ld32(tmem + lane_off + C::COL_DQ + 32 * cc, r);
+            // Drain dQ from tensor memory 64 columns per wait; the columns are
+            // handed back to the MMA issuer before the last reductions go out.
+#pragma unroll 1
+            for (int cc = 0; cc < D / 64; ++cc) {
+                uint32_t r0[32], r1[32];
+                ptx::tmem_ld32(tmem + lane_off + C::COL_DQ + 64 * cc, r0);
+                ptx::tmem_ld32(tmem + lane_off + C::COL_DQ + 64 * cc + 32, r1);
                 ptx::tmem_ld_wait();
+                if (cc == D / 64 - 1) {
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(BAR(B_DQ_EMPTY));
+                }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const float4 v4 = make_float4(__uint_as_float(r[4 * e]), __uint_as_float(r[4 * e + 1]),
-                                                  __uint_as_float(r[4 * e + 2]), __uint_as_float(r[4 * e + 3]));
-                    atomicAdd(reinterpret_cast<float4*>(gdq + 32 * cc + 4 * e), v4);
-                    if (gpart) *reinterpret_cast<float4*>(gpart + 32 * cc + 4 * e) = v4;
+                    float* g = gdq + 64 * cc + 4 * e;
+                    ptx::red_add_v4(g, __uint_as_float(r0[4 * e]), __uint_as_float(r0[4 * e + 1]),
+                                    __uint_as_float(r0[4 * e + 2]), __uint_as_float(r0[4 * e + 3]));
+                    ptx::red_add_v4(g + 32, __uint_as_float(r1[4 * e]), __uint_as_float(r1[4 * e + 1]),
+                                    __uint_as_float(r1[4 * e + 2]), __uint_as_float(r1[4 * e + 3]));
+                    if (gpart) {
+                        float* gp = gpart + 64 * cc + 4 * e;
+                        *reinterpret_cast<float4*>(gp) =
+                            make_float4(__uint_as_float(r0[4 * e]), __uint_as_float(r0[4 * e + 1]),
+                                        __uint_as_float(r0[4 * e + 2]), __uint_as_float(r0[4 * e + 3]));
+                        *reinterpret_cast<float4*>(gp + 32) =
+                            make_float4(__uint_as_float(r1[4 * e]), __uint_as_float(r1[4 * e + 1]),
+                                        __uint_as_float(r1[4 * e + 2]), __uint_as_float(r1[4 * e + 3]));
+                    }
                 }
             }
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(BAR(B_DQ_EMPTY));
             if (ordered || p.order_log) {
                 __threadfence();
                 ptx::named_bar_sync(1, 128);
