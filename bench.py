@@ -43,6 +43,10 @@ def parse():
     ap.add_argument("--impl", default="dash", choices=["dash", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--wait-profile", action="store_true",
+                    help="one step of --schedule with the kernel's per-role wait-cycle counters; prints a JSON line")
+    ap.add_argument("--trace-out", default=None,
+                    help="with --wait-profile: also write the event trace of CTA 0 (JSON) to this path")
     ap.add_argument("--kernel-only", action="store_true",
                     help="only W + K steps of --schedule (for profiler captures); prints a short JSON line")
     return ap.parse_args()
@@ -218,6 +222,10 @@ def main_gpu(args):
     if args.schedule:
         det = [args.schedule]
 
+    if args.wait_profile:
+        print(json.dumps(wait_profile(w, args.schedule or det[0], tensors, outs, args.warmup, stream,
+                                      args.trace_out)))
+        return
     if args.kernel_only:
         sched = args.schedule or det[0]
         ms, _, lps = time_schedule(w, sched, tensors, outs, args.steps, args.warmup, stream)
@@ -301,6 +309,48 @@ def main_gpu(args):
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+
+
+WAIT_SITES = {
+    "drain": {0: "wait pair descriptor", 1: "wait dQ in TMEM", 2: "wait dK/dV done", 3: "wait staging buffer",
+              8: "stage dQ (incl. waits)"},
+    "producer": {0: "wait descriptor slot", 1: "wait K/V buffer free", 2: "wait Q stage free", 3: "wait dO buffer free"},
+    "mma": {0: "wait first descriptor/K/V/Q", 1: "wait next K/V", 2: "wait first dO", 3: "wait P ready",
+            4: "wait dK/dV drained", 5: "wait next descriptor", 6: "wait next Q", 7: "wait dS ready",
+            8: "wait dQ columns free", 9: "wait next dO"},
+    "softmax": {0: "wait pair descriptor", 1: "wait S", 2: "wait dP", 3: "wait dS buffer free",
+                8: "compute P (ld S, exp, st P)", 9: "compute dS (ld dP, math)"},
+    "issuer": {0: "wait pair descriptor", 1: "wait staged dQ", 2: "wait reduce complete + release",
+               8: "wait accumulation turn", 9: "issue TMA reduce + smem read"},
+}
+
+
+def wait_profile(w, sched, tensors, outs, warmup, stream, trace_out=None):
+    """Mean fraction of each CTA's cycles spent in each wait / phase."""
+    import torch
+    from tile_scheduling_persistent_gb300 import dash
+    q, k, v, o, do, lse = tensors
+    dq, dqb, dk, dv = outs
+    P = dash.num_ctas()
+    cyc = torch.zeros(P, 64, dtype=torch.int64, device=q.device)
+    for _ in range(warmup):
+        dash.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, w.causal, sched, stream=stream)
+    trace = torch.zeros(64, 32, dtype=torch.int64, device=q.device) if trace_out else None
+    dash.attn_bwd_debug(q, k, v, o, do, lse, dq, dk, dv, w.causal, sched, stream=stream, wait_cycles=cyc,
+                        event_trace=trace)
+    torch.cuda.synchronize()
+    if trace_out:
+        with open(trace_out, "w") as f:
+            json.dump({"workload": w.name, "schedule": sched, "trace": trace.cpu().tolist()}, f)
+    c = cyc.double().cpu()
+    total = c[:, 63]
+    busy = total > 0
+    out = {"workload": w.name, "schedule": sched, "ctas": int(busy.sum()),
+           "mean_cta_cycles": float(total[busy].mean())}
+    for r, role in enumerate(("drain", "producer", "mma", "softmax", "issuer")):
+        out[role] = {name: round(float((c[busy, r * 10 + site] / total[busy]).mean()), 4)
+                     for site, name in WAIT_SITES[role].items()}
+    return out
 
 
 def e2e_run(w, sched, tensors, steps, warmup, stream):

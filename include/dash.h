@@ -199,6 +199,16 @@ typedef struct {
      * after the persistent kernel's launch (for timing that kernel alone). */
     void* kernel_event_begin;
     void* kernel_event_end;
+    /* device uint64 [P][64] or NULL: per-CTA clock64 cycles spent in each
+     * wait / phase of the persistent kernel, slot = role*10 + site (role 0
+     * dQ drain, 1 producer, 2 MMA issuer, 3 softmax/dS, 4 reduce issuer);
+     * slot 63 = the CTA's total cycles.  Sites are named in the kernel
+     * source.  Selects an instrumented build of the kernel. */
+    unsigned long long* wait_cycles;
+    /* device uint64 [64][32] or NULL (needs wait_cycles): clock64 of named
+     * events (MMA issues, softmax/drain/reduce milestones) for the first 64
+     * pairs of CTA 0; event ids are listed in the kernel source. */
+    unsigned long long* event_trace;
 } dash_debug_opts;
 
 /* dash_attn_bwd with debug hooks; same arguments and errors, plus

@@ -188,7 +188,8 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
     BwdParams prm;
     memset(&prm, 0, sizeof(prm));
     if (make_tmap_2d(&prm.tm_q, q, (long long)B * Hq * S, D) || make_tmap_2d(&prm.tm_k, k, (long long)B * Hkv * S, D) ||
-        make_tmap_2d(&prm.tm_v, v, (long long)B * Hkv * S, D) || make_tmap_2d(&prm.tm_do, dO, (long long)B * Hq * S, D))
+        make_tmap_2d(&prm.tm_v, v, (long long)B * Hkv * S, D) || make_tmap_2d(&prm.tm_do, dO, (long long)B * Hq * S, D) ||
+        make_tmap_2d_f32(&prm.tm_dq, dq, (long long)B * Hq * S, D))
         return DASH_ERR_CUDA;
     prm.lse = lse;
     prm.delta = (const float*)ws->delta.p;
@@ -206,6 +207,9 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
         prm.partials = dbg->dq_partials;
         prm.cta_perm = dbg->cta_perm;
         prm.delay_ns = dbg->start_delay_ns;
+        prm.prof = dbg->wait_cycles;
+        prm.trace = dbg->event_trace;
+        if (prm.trace && !prm.prof) return DASH_ERR_ARG;   // the trace needs the instrumented build
     }
     prm.timeout_ns = g_timeout_ns.load();
     prm.ntasks = ntasks;
@@ -233,17 +237,30 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
 
 }  // namespace
 
-int make_tmap_2d(void* map_out, const void* base, long long rows, int D) {
+namespace {
+int encode_2d(void* map_out, CUtensorMapDataType dt, int esize, const void* base, long long rows, int D,
+              unsigned box_cols) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return -2;
     const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-    const cuuint32_t box[2] = {64, 128};
+    const cuuint64_t strides[1] = {(cuuint64_t)D * esize};
+    const cuuint32_t box[2] = {box_cols, 128};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(reinterpret_cast<CUtensorMap*>(map_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
-                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(reinterpret_cast<CUtensorMap*>(map_out), dt, 2, const_cast<void*>(base), dims, strides, box,
+                    estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? 0 : -2;
+}
+}  // namespace
+
+// bf16 [rows, D], boxes of 64 columns x 128 rows (128 B rows, swizzled).
+int make_tmap_2d(void* map_out, const void* base, long long rows, int D) {
+    return encode_2d(map_out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, rows, D, 64);
+}
+
+// fp32 [rows, D], boxes of 32 columns x 128 rows (128 B rows, swizzled).
+int make_tmap_2d_f32(void* map_out, const void* base, long long rows, int D) {
+    return encode_2d(map_out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, rows, D, 32);
 }
 
 }  // namespace dash

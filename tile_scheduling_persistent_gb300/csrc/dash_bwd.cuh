@@ -23,11 +23,16 @@
 // section 1: a fixed accumulation order makes dQ reproducible).
 //
 // Warp roles (16 warps, 512 threads):
-//   warps 0-3   reducer: drain dQ from TMEM, ordered fp32 reduction into
-//               global dq, and the dK/dV epilogue of each KV tile;
+//   warps 0-3   drain: read dQ out of tensor memory into a swizzled fp32
+//               staging buffer in shared memory, and the dK/dV epilogue of
+//               each KV tile;
 //   warp 4      producer: task dispatch, pair descriptors, TMA loads;
 //   warp 5      MMA issuer (one thread) and TMEM owner;
-//   warps 6-7   idle;
+//   warp 6      reduce issuer (one thread): waits for the pair's turn, adds
+//               the staged dQ partial into global dq with TMA reduce-add
+//               (cp.reduce.async.bulk.tensor), waits for completion, releases
+//               the turn;
+//   warp 7      idle;
 //   warps 8-15  softmax / dS: warp w owns TMEM lanes 32*(w%4).. and the Q
 //               columns 64*((w-8)/4) .. +63 of the pair.
 //
@@ -37,8 +42,8 @@
 //
 // Every wait is bounded (%globaltimer); a wait that runs out records the
 // failure in the status word, raises a CTA-wide and a grid-wide abort flag,
-// and every role then leaves its loop; the CTA waits for its own TMA loads
-// and MMAs to land, frees tensor memory and exits.
+// and every role then leaves its loop; the CTA waits for its own TMA loads,
+// reductions and MMAs to land, frees tensor memory and exits.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -52,10 +57,9 @@ namespace dash {
 constexpr int kThreads = 512;
 constexpr int kBox = 16384;        // 128 rows x 128 B
 constexpr int kNDesc = 8;          // pair-descriptor ring depth
-constexpr int kStages = 2;         // Q/dO/LSE/delta stages
 constexpr float kLog2e = 1.4426950408889634f;
 
-enum Role : int { kRoleReducer = 0, kRoleProducer = 1, kRoleMma = 2, kRoleSoftmax = 3 };
+enum Role : int { kRoleReducer = 0, kRoleProducer = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleIssuer = 4 };
 enum DescFlags : int { kKvFirst = 1, kKvLast = 2, kDiag = 4, kEnd = 8 };
 
 // Barrier slots (8 bytes each) at the start of the control area.
@@ -65,8 +69,10 @@ enum Bar : int {
     B_KV_FULL = B_DESC_EMPTY + kNDesc,
     B_KV_EMPTY,
     B_Q_FULL,
-    B_Q_EMPTY = B_Q_FULL + kStages,
-    B_S_FULL = B_Q_EMPTY + kStages,
+    B_Q_EMPTY = B_Q_FULL + 2,
+    B_DO_FULL = B_Q_EMPTY + 2,
+    B_DO_EMPTY = B_DO_FULL + 2,
+    B_S_FULL = B_DO_EMPTY + 2,
     B_DP_FULL,
     B_P_READY,
     B_DS_READY,
@@ -75,36 +81,59 @@ enum Bar : int {
     B_DQ_EMPTY,
     B_ACC_FULL,
     B_ACC_EMPTY,
+    B_STG_FULL,
+    B_STG_EMPTY,
     B_DRAIN,
     B_COUNT
 };
 
-static_assert(B_COUNT * 8 <= 256, "barrier area");
+// Control area: barriers [0, 320), descriptors [320, 576), TMEM address
+// 576, abort flag 580, cycle counters [584, 992).
+constexpr int kCtlBars = 0, kCtlDescs = 320, kCtlTmem = 576, kCtlAbort = 580, kCtlProf = 584;
+constexpr int kProfPerRole = 10;
+constexpr int kProfSmem = 5 * kProfPerRole + 1;   // + whole-CTA cycles
+constexpr int kProfOut = 64;                       // per-CTA entries in the debug buffer
+constexpr int kTracePairs = 64;                    // event trace of the first pairs of CTA 0
+constexpr int kTraceEvents = 32;
+enum TraceEv : int {
+    EV_S_ISSUE = 0, EV_DP_ISSUE, EV_DV_ISSUE, EV_DK_ISSUE, EV_DQ_ISSUE,         // MMA issuer
+    EV_SM_S_SEEN = 5, EV_SM_P_DONE, EV_SM_DP_SEEN, EV_SM_DS_DONE,               // softmax warp 8
+    EV_DR_DQ_SEEN = 10, EV_DR_DQ_EMPTY, EV_DR_STAGED0, EV_DR_STAGED1,           // drain warp 0
+    EV_IS_STG_SEEN = 15, EV_IS_TURN, EV_IS_READ0, EV_IS_READ1, EV_IS_DONE,      // reduce issuer
+    EV_PR_DESC = 22, EV_PR_Q_ISSUED, EV_PR_DO_ISSUED                            // producer
+};
+static_assert(B_COUNT * 8 <= kCtlDescs, "barrier area");
+static_assert(kCtlProf + kProfSmem * 8 <= 1024, "control area");
 
 struct PairDesc {
     int b, hq, hkv, q, kv, flags, rank, pad;
 };
-static_assert(sizeof(PairDesc) * kNDesc <= 256, "descriptor ring area");
+static_assert(sizeof(PairDesc) * kNDesc <= kCtlTmem - kCtlDescs, "descriptor ring area");
 
 template <int D>
 struct Cfg {
     static constexpr int kTile = D * 128 * 2;         // 128 x D bf16
     static constexpr int kNBox = D / 64;
+    static constexpr int kQStages = 2;
+    static constexpr int kDoStages = (D == 128) ? 1 : 2;   // dO's last use (dV) comes early
+    static constexpr int kHalves = D / 64;             // staging passes per dQ tile (64 fp32 columns each)
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + kTile;
-    static constexpr int OFF_STAGE = OFF_V + kTile;    // stage s: Q at +2s*kTile, dO at +(2s+1)*kTile
-    static constexpr int OFF_DS = OFF_STAGE + kStages * 2 * kTile;
-    static constexpr int OFF_VEC = OFF_DS + 2 * kBox;  // per stage: LSE[128], delta[128]
-    static constexpr int OFF_CTL = OFF_VEC + kStages * 1024;
-    static constexpr int CTL_BYTES = 1024;             // barriers, descriptors, flags
-    static constexpr int kSmem = OFF_CTL + CTL_BYTES;
+    static constexpr int OFF_Q = OFF_V + kTile;
+    static constexpr int OFF_DO = OFF_Q + kQStages * kTile;
+    static constexpr int OFF_DS = OFF_DO + kDoStages * kTile;
+    static constexpr int OFF_STG = OFF_DS + 2 * kBox;  // fp32 staging: 2 boxes of 128 rows x 32 floats
+    static constexpr int OFF_VEC = OFF_STG + 2 * kBox; // per Q stage: LSE[128], delta[128]
+    static constexpr int OFF_CTL = OFF_VEC + kQStages * 1024;
+    static constexpr int kSmem = OFF_CTL + 1024;
     static constexpr uint32_t COL_DK = 0;
     static constexpr uint32_t COL_DV = D;
     static constexpr uint32_t COL_S = 2 * D;
     static constexpr uint32_t COL_DP = 2 * D + 128;
     static constexpr bool kDqAlias = (D == 128);
     static constexpr uint32_t COL_DQ = kDqAlias ? COL_DP : 2 * D + 256;
-    static constexpr uint32_t kStageBytes = 2 * kTile + 1024;
+    static constexpr uint32_t kQBytes = kTile + 1024;   // Q tile + LSE + delta
+    static constexpr uint32_t kDoBytes = kTile;
     static constexpr uint32_t kKvBytes = 2 * kTile;
     static_assert(kSmem <= 232448, "shared memory budget");
     static_assert(COL_DQ + D <= 512, "tensor memory budget");
@@ -112,6 +141,7 @@ struct Cfg {
 
 struct BwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;   // 2D [rows, D] bf16, box 64 x 128, SWIZZLE_128B
+    CUtensorMap tm_dq;                      // 2D [rows, D] fp32, box 32 x 128, SWIZZLE_128B
     const float* lse;
     const float* delta;
     float* dq;
@@ -127,6 +157,8 @@ struct BwdParams {
     float* partials;                        // debug, may be null
     const int32_t* cta_perm;                // debug, may be null
     const int64_t* delay_ns;                // debug, may be null
+    unsigned long long* prof;               // debug, may be null: [P][kProfOut] cycle counters
+    unsigned long long* trace;              // debug, may be null: [kTracePairs][kTraceEvents] clock64 of CTA 0
     unsigned long long timeout_ns;
     long long ntasks;
     int B, Hq, Hkv, S, n, G, causal, sched, P;
@@ -236,6 +268,17 @@ __device__ __forceinline__ void ds_64(uint32_t tmem_dp_lane, int c0, const float
             __nv_bfloat162 h2 = __floats2bfloat162_rn(d0, d1);
             pk[16 * half + k] = *reinterpret_cast<uint32_t*>(&h2);
         }
+    }
+}
+
+// 32 fp32 values of one row into a 128-byte-swizzled fp32 box (128 rows x
+// 32 floats): chunk c of 4 floats lands at (c ^ (row % 8)) in the row.
+__device__ __forceinline__ void store_row_f32_sw128(uint8_t* box, int row, const uint32_t (&r)[32]) {
+    uint8_t* rp = box + row * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint4 v = make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
+        *reinterpret_cast<uint4*>(rp + ((c ^ (row & 7)) << 4)) = v;
     }
 }
 

@@ -38,7 +38,8 @@ class _DebugOpts(ctypes.Structure):
     _fields_ = [("order_log", ctypes.c_void_p), ("dq_partials", ctypes.c_void_p), ("cta_perm", ctypes.c_void_p),
                 ("start_delay_ns", ctypes.c_void_p), ("ranks_host", ctypes.c_void_p),
                 ("skip_table_check", ctypes.c_int), ("kernel_event_begin", ctypes.c_void_p),
-                ("kernel_event_end", ctypes.c_void_p)]
+                ("kernel_event_end", ctypes.c_void_p), ("wait_cycles", ctypes.c_void_p),
+                ("event_trace", ctypes.c_void_p)]
 
 
 _lib = None
@@ -117,8 +118,10 @@ def attn_bwd(q, k, v, o, do, lse, dq, dk, dv, causal, schedule, stream=None):
 
 def attn_bwd_debug(q, k, v, o, do, lse, dq, dk, dv, causal, schedule, stream=None, order_log=None,
                    dq_partials=None, cta_perm=None, start_delay_ns=None, ranks_host=None, skip_table_check=False,
-                   kernel_events=None):
+                   kernel_events=None, wait_cycles=None, event_trace=None):
     opts = _DebugOpts()
+    opts.wait_cycles = _ptr(wait_cycles, torch.int64)
+    opts.event_trace = _ptr(event_trace, torch.int64)
     if kernel_events is not None:
         opts.kernel_event_begin = ctypes.c_void_p(kernel_events[0].cuda_event)
         opts.kernel_event_end = ctypes.c_void_p(kernel_events[1].cuda_event)
