@@ -312,16 +312,13 @@ def main_gpu(args):
 
 
 WAIT_SITES = {
-    "drain": {0: "wait pair descriptor", 1: "wait dQ in TMEM", 2: "wait dK/dV done", 3: "wait staging buffer",
-              8: "stage dQ (incl. waits)"},
-    "producer": {0: "wait descriptor slot", 1: "wait K/V buffer free", 2: "wait Q stage free", 3: "wait dO buffer free"},
+    "drain": {0: "wait pair descriptor", 1: "wait dQ in TMEM", 2: "wait dK/dV done", 8: "wait accumulation turn"},
+    "producer": {0: "wait descriptor slot", 1: "wait K/V buffer free", 2: "wait Q stage free", 3: "wait dO stage free"},
     "mma": {0: "wait first descriptor/K/V/Q", 1: "wait next K/V", 2: "wait first dO", 3: "wait P ready",
             4: "wait dK/dV drained", 5: "wait next descriptor", 6: "wait next Q", 7: "wait dS ready",
             8: "wait dQ columns free", 9: "wait next dO"},
     "softmax": {0: "wait pair descriptor", 1: "wait S", 2: "wait dP", 3: "wait dS buffer free",
-                8: "compute P (ld S, exp, st P)", 9: "compute dS (ld dP, math)"},
-    "issuer": {0: "wait pair descriptor", 1: "wait staged dQ", 2: "wait reduce complete + release",
-               8: "wait accumulation turn", 9: "issue TMA reduce + smem read"},
+                8: "compute P (ld S, exp, st P)", 9: "compute + store dS"},
 }
 
 
@@ -347,7 +344,7 @@ def wait_profile(w, sched, tensors, outs, warmup, stream, trace_out=None):
     busy = total > 0
     out = {"workload": w.name, "schedule": sched, "ctas": int(busy.sum()),
            "mean_cta_cycles": float(total[busy].mean())}
-    for r, role in enumerate(("drain", "producer", "mma", "softmax", "issuer")):
+    for r, role in enumerate(("drain", "producer", "mma", "softmax")):
         out[role] = {name: round(float((c[busy, r * 10 + site] / total[busy]).mean()), 4)
                      for site, name in WAIT_SITES[role].items()}
     return out

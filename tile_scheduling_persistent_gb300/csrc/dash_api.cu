@@ -66,7 +66,8 @@ struct DevBuf {
     }
 };
 
-// ints layout: [0..7] status, [8] task counter, [9] abort, [16 .. 16+T) sem, [16+T .. 16+2T) log cursors
+// ints layout: [0..7] status, [8] task counter, [9] abort, then the
+// accumulation counters [T][kSubTiles] and the order-log cursors [T].
 constexpr int kIntHeader = 16;
 
 struct Workspace {
@@ -154,7 +155,7 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
 
     Workspace* ws = get_ws(dev, stream);
     if (ws->delta.ensure((size_t)tiles * 128 * sizeof(float)) ||
-        ws->ints.ensure((size_t)(kIntHeader + 2 * tiles) * sizeof(int)))
+        ws->ints.ensure((size_t)(kIntHeader + (kSubTiles + 1) * tiles) * sizeof(int)))
         return DASH_ERR_NOMEM;
 
     const uint16_t* ranks = nullptr;
@@ -180,7 +181,7 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
     }
 
     int* ints = (int*)ws->ints.p;
-    if (cudaMemsetAsync(ints, 0, (size_t)(kIntHeader + 2 * tiles) * sizeof(int), stream) != cudaSuccess ||
+    if (cudaMemsetAsync(ints, 0, (size_t)(kIntHeader + (kSubTiles + 1) * tiles) * sizeof(int), stream) != cudaSuccess ||
         cudaMemsetAsync(dq, 0, (size_t)tiles * 128 * D * sizeof(float), stream) != cudaSuccess)
         return DASH_ERR_CUDA;
     if (launch_preprocess(o, dO, (float*)ws->delta.p, tiles * 128, D, stream)) return DASH_ERR_CUDA;
@@ -188,8 +189,7 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
     BwdParams prm;
     memset(&prm, 0, sizeof(prm));
     if (make_tmap_2d(&prm.tm_q, q, (long long)B * Hq * S, D) || make_tmap_2d(&prm.tm_k, k, (long long)B * Hkv * S, D) ||
-        make_tmap_2d(&prm.tm_v, v, (long long)B * Hkv * S, D) || make_tmap_2d(&prm.tm_do, dO, (long long)B * Hq * S, D) ||
-        make_tmap_2d_f32(&prm.tm_dq, dq, (long long)B * Hq * S, D))
+        make_tmap_2d(&prm.tm_v, v, (long long)B * Hkv * S, D) || make_tmap_2d(&prm.tm_do, dO, (long long)B * Hq * S, D))
         return DASH_ERR_CUDA;
     prm.lse = lse;
     prm.delta = (const float*)ws->delta.p;
@@ -201,7 +201,7 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
     prm.task_counter = ints + 8;
     prm.abort_flag = ints + 9;
     prm.sem = ints + kIntHeader;
-    prm.logcnt = ints + kIntHeader + tiles;
+    prm.logcnt = ints + kIntHeader + kSubTiles * tiles;
     if (dbg) {
         prm.order_log = dbg->order_log;
         prm.partials = dbg->dq_partials;

@@ -84,10 +84,9 @@ __device__ __forceinline__ int64_t next_task(const BwdParams& p, int slot, int& 
     return (int64_t)atomicAdd(p.task_counter, 1);
 }
 
-// Spin until the accumulation counter of a dQ tile equals `rank` (acquire).
-__device__ bool wait_turn(const BwdParams& p, const Ctl& c, volatile int* abort_smem, int tile, int rank,
-                          int head) {
-    int* sem = p.sem + tile;
+// Spin until an accumulation counter equals `rank` (acquire).
+__device__ bool wait_turn(const BwdParams& p, const Ctl& c, volatile int* abort_smem, int* sem, int rank, int head,
+                          int qtile) {
     if (ptx::ld_acquire(sem) == rank) return true;
     const uint64_t t0 = ptx::globaltimer();
     int spins = 0;
@@ -96,11 +95,11 @@ __device__ bool wait_turn(const BwdParams& p, const Ctl& c, volatile int* abort_
         if ((++spins & 63) == 0) {
             if (ptx::ld_volatile(p.abort_flag) || *abort_smem) return false;
             if (ptx::globaltimer() - t0 > c.timeout) {
-                report_timeout(c, kRoleReducer, head, tile % p.n, rank);
+                report_timeout(c, kRoleDrain, head, qtile, rank);
                 return false;
             }
         }
-        __nanosleep(64);
+        __nanosleep(32);
     }
 }
 
@@ -112,6 +111,7 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int wg = warp >> 2;
 
     uint8_t* ctl = smem + C::OFF_CTL;
     const uint32_t bar0 = ptx::smem_u32(ctl + kCtlBars);
@@ -122,8 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
     unsigned long long* prof_smem = reinterpret_cast<unsigned long long*>(ctl + kCtlProf);
 
     constexpr bool prof_on = kProf;   // cycle counters compiled in only for the debug instantiation
-    const bool prof_rec =
-        prof_on && lane == 0 && (warp == 0 || warp == 4 || warp == 5 || warp == 6 || warp == 8);
+    const bool prof_rec = prof_on && lane == 0 && (warp == 0 || warp == 1 || warp == 4 || warp == 8);
     const Ctl c{abort_smem, p.status, p.abort_flag, p.timeout_ns, prof_rec ? prof_smem : nullptr};
     const unsigned long long t_start = kProf ? clock64() : 0ull;
     const uint32_t sbase = ptx::smem_u32(smem);
@@ -133,13 +132,13 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
         if (sbase & 1023u) report_timeout(c, -1, (int)sbase, 0, 0);
         for (int i = 0; i < kNDesc; ++i) {
             ptx::mbar_init(BAR(B_DESC_FULL + i), 1);
-            ptx::mbar_init(BAR(B_DESC_EMPTY + i), 1);
+            ptx::mbar_init(BAR(B_DESC_EMPTY + i), kSubTiles);   // the drain warps read it last
         }
         ptx::mbar_init(BAR(B_KV_FULL), 1);
         ptx::mbar_init(BAR(B_KV_EMPTY), 1);
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(BAR(B_Q_FULL + s), 1);
-            ptx::mbar_init(BAR(B_Q_EMPTY + s), 9);   // MMA commit + 8 softmax warps (LSE/delta)
+            ptx::mbar_init(BAR(B_Q_EMPTY + s), 1);
             ptx::mbar_init(BAR(B_DO_FULL + s), 1);
             ptx::mbar_init(BAR(B_DO_EMPTY + s), 1);
         }
@@ -149,17 +148,15 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
         ptx::mbar_init(BAR(B_DS_READY), 8);
         ptx::mbar_init(BAR(B_DS_FREE), 1);
         ptx::mbar_init(BAR(B_DQ_FULL), 1);
-        ptx::mbar_init(BAR(B_DQ_EMPTY), 4);
+        ptx::mbar_init(BAR(B_DQ_EMPTY), kSubTiles);
         ptx::mbar_init(BAR(B_ACC_FULL), 1);
-        ptx::mbar_init(BAR(B_ACC_EMPTY), 4);
-        ptx::mbar_init(BAR(B_STG_FULL), 4);
-        ptx::mbar_init(BAR(B_STG_EMPTY), 1);
+        ptx::mbar_init(BAR(B_ACC_EMPTY), 8);
         ptx::mbar_init(BAR(B_DRAIN), 1);
         ptx::fence_mbar_init();
         if (prof_on)
             for (int i = 0; i < kProfSmem; ++i) prof_smem[i] = 0;
     }
-    if (warp == 5) {
+    if (warp == 1) {
         ptx::tmem_alloc(ptx::smem_u32((const void*)tmem_slot), 512);
         ptx::tmem_relinquish();
     }
@@ -171,7 +168,11 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
     const Shape sh{p.B, p.Hq, p.Hkv, p.n, p.G, p.causal, p.sched};
     const bool ordered = is_ordered(p.sched);
 
-    if (warp == 4) {
+    // Each warpgroup first re-sizes its registers (all four warps execute the
+    // same setmaxnreg), then runs its role.
+    if (wg == 0) {
+    ptx::setmaxnreg_dec<Regs<D>::kCtl>();
+    if (warp == 0) {
         // ================================================== producer
         if (lane == 0 && !*abort_smem) {
             ptx::prefetch_tensormap(&p.tm_q);
@@ -241,7 +242,6 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                         ++kvc;
                     }
                     const int qrow = (v.b * p.Hq + v.hq) * p.S + v.q * 128;
-                    // Q, LSE, delta
                     const int st = (int)(pc % C::kQStages);
                     if (q_armed[st] > 0 && !wait1(BAR(B_Q_EMPTY + st), (uint32_t)((q_armed[st] - 1) & 1), c,
                                                   kRoleProducer, (int)pc, 2)) {
@@ -253,12 +253,8 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                     const uint32_t sq = sbase + C::OFF_Q + st * C::kTile;
 #pragma unroll
                     for (int bx = 0; bx < C::kNBox; ++bx) ptx::tma_load_2d(sq + bx * kBox, &p.tm_q, 64 * bx, qrow, fb);
-                    const uint32_t sv = sbase + C::OFF_VEC + st * 1024;
-                    ptx::bulk_load(sv, p.lse + qrow, 512, fb);
-                    ptx::bulk_load(sv + 512, p.delta + qrow, 512, fb);
                     ++q_armed[st];
                     trace_ev<kProf>(p, pc, EV_PR_Q_ISSUED);
-                    // dO
                     const int so = (int)(pc % C::kDoStages);
                     if (do_armed[so] > 0 && !wait1(BAR(B_DO_EMPTY + so), (uint32_t)((do_armed[so] - 1) & 1), c,
                                                    kRoleProducer, (int)pc, 3)) {
@@ -291,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                 drain(BAR(B_DO_FULL + s), do_armed[s]);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 1) {
         // ================================================== MMA issuer
         if (lane == 0 && !*abort_smem) {
             const uint32_t tS = tmem + C::COL_S, tDP = tmem + C::COL_DP, tDQ = tmem + C::COL_DQ;
@@ -352,6 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                     if (!wait1(BAR(B_DS_READY), (uint32_t)(pp & 1), c, kRoleMma, (int)pp, 7)) break;
                     ptx::tc_fence_after();
                     issue_dk<D>(tDK, sDS, sQ(pp), kv_first ? 0u : 1u);
+                    ptx::tc_commit(BAR(B_Q_EMPTY + (int)(pp % C::kQStages)));
                     trace_ev<kProf>(p, pp, EV_DK_ISSUE);
                     if (!C::kDqAlias && pp > 0 &&
                         !wait1(BAR(B_DQ_EMPTY), (uint32_t)((pp - 1) & 1), c, kRoleMma, (int)pp, 8))
@@ -361,7 +358,6 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                     trace_ev<kProf>(p, pp, EV_DQ_ISSUE);
                     ptx::tc_commit(BAR(B_DS_FREE));
                     ptx::tc_commit(BAR(B_DQ_FULL));
-                    ptx::tc_commit(BAR(B_Q_EMPTY + (int)(pp % C::kQStages)));
                     if (d.flags & kKvLast) {
                         ptx::tc_commit(BAR(B_ACC_FULL));
                         ptx::tc_commit(BAR(B_KV_EMPTY));
@@ -392,186 +388,193 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
             while (!ptx::mbar_try_wait(BAR(B_DRAIN), 0) && ptx::globaltimer() - t0 < 100000000ull) {
             }
         }
-    } else if (warp == 6) {
-        // ================================================== reduce issuer
-        if (lane == 0 && !*abort_smem) {
-            ptx::prefetch_tensormap(&p.tm_dq);
-            const uint32_t sstg = sbase + C::OFF_STG;
-            long long u = 0;   // staging-buffer uses
-            for (long long pp = 0;; ++pp) {
-                const int ds = (int)(pp % kNDesc);
-                if (!wait1(BAR(B_DESC_FULL + ds), (uint32_t)((pp / kNDesc) & 1), c, kRoleIssuer, (int)pp, 0)) break;
-                const PairDesc d = descs[ds];
-                if (d.flags & kEnd) break;
-                const int tile = (d.b * p.Hq + d.hq) * p.n + d.q;
-                const int row0 = (d.b * p.Hq + d.hq) * p.S + d.q * 128;
-                bool ok = true;
-                for (int h = 0; h < C::kHalves; ++h) {
-                    if (!wait1(BAR(B_STG_FULL), (uint32_t)(u & 1), c, kRoleIssuer, (int)pp, 1)) {
-                        ok = false;
-                        break;
-                    }
-                    if (h == 0) trace_ev<kProf>(p, pp, EV_IS_STG_SEEN);
-                    if (h == 0) {
-                        const unsigned long long t0 = kProf ? clock64() : 0ull;
-                        if (ordered && !wait_turn(p, c, abort_smem, tile, d.rank, d.b * p.Hq + d.hq)) {
-                            ok = false;
-                            break;
-                        }
-                        prof_add(c, kRoleIssuer, 8, t0);
-                        trace_ev<kProf>(p, pp, EV_IS_TURN);
-                        if (p.order_log) {
-                            const int s = atomicAdd(p.logcnt + tile, 1);
-                            if (s >= 0 && s < p.n) p.order_log[(size_t)tile * p.n + s] = d.kv;
-                        }
-                        ptx::fence_proxy_async_global();
-                    }
-                    const unsigned long long t1 = kProf ? clock64() : 0ull;
-                    ptx::tma_reduce_add_2d(&p.tm_dq, 64 * h, row0, sstg);
-                    ptx::tma_reduce_add_2d(&p.tm_dq, 64 * h + 32, row0, sstg + kBox);
-                    ptx::bulk_commit();
-                    ptx::bulk_wait_read0();
-                    trace_ev<kProf>(p, pp, EV_IS_READ0 + (h & 1));
-                    prof_add(c, kRoleIssuer, 9, t1);
-                    ptx::mbar_arrive(BAR(B_STG_EMPTY));
-                    ++u;
-                }
-                if (!ok) break;
-                if (ordered) {
-                    const unsigned long long t2 = kProf ? clock64() : 0ull;
-                    ptx::bulk_wait0();
-                    ptx::fence_proxy_async_global();
-                    ptx::st_release(p.sem + tile, d.rank + 1);
-                    prof_add(c, kRoleIssuer, 2, t2);
-                }
-                trace_ev<kProf>(p, pp, EV_IS_DONE);
-                ptx::mbar_arrive(BAR(B_DESC_EMPTY + ds));
-            }
-            ptx::bulk_wait0();
-        }
-    } else if (warp >= 8) {
+    }
+    } else if (wg == 2 || wg == 3) {
+        ptx::setmaxnreg_inc<Regs<D>::kSoftmax>();
         // ================================================== softmax / dS
         const int sub = warp & 3;
-        const int c0 = 64 * ((warp - 8) >> 2);
+        const int c0 = 64 * (wg - 2);
         const int row = 32 * sub + lane;                   // KV row within the tile
         const uint32_t lane_off = (uint32_t)(32 * sub) << 16;
         uint8_t* ds_box = smem + C::OFF_DS + (c0 >> 6) * kBox;
+        const bool rec = warp == 8 && lane == 0;
         for (long long pp = 0;; ++pp) {
             const int ds = (int)(pp % kNDesc);
             if (!waitw(BAR(B_DESC_FULL + ds), (uint32_t)((pp / kNDesc) & 1), c, kRoleSoftmax, (int)pp, 0)) break;
             const PairDesc d = descs[ds];
             if (d.flags & kEnd) break;
-            const int st = (int)(pp % C::kQStages);
-            const float* vec = reinterpret_cast<const float*>(smem + C::OFF_VEC + st * 1024);
+            // per-column statistics of this pair's Q tile: lane l holds columns c0+l and c0+32+l
+            const size_t qrow = (size_t)(d.b * p.Hq + d.hq) * p.S + (size_t)d.q * 128 + c0 + lane;
+            const float lse2_a = ptx::ld_nc(p.lse + qrow) * kLog2e;
+            const float lse2_b = ptx::ld_nc(p.lse + qrow + 32) * kLog2e;
+            const float delta_a = ptx::ld_nc(p.delta + qrow);
+            const float delta_b = ptx::ld_nc(p.delta + qrow + 32);
             if (!waitw(BAR(B_S_FULL), (uint32_t)(pp & 1), c, kRoleSoftmax, (int)pp, 1)) break;
-            if (warp == 8 && lane == 0) trace_ev<kProf>(p, pp, EV_SM_S_SEEN);
+            if (rec) trace_ev<kProf>(p, pp, EV_SM_S_SEEN);
             ptx::tc_fence_after();
             float P[64];
             unsigned long long tc0 = kProf ? clock64() : 0ull;
-            softmax_64(tmem + lane_off + C::COL_S, c0, vec, p.scale_log2e, (d.flags & kDiag) != 0, row, P);
+            softmax_64(tmem + lane_off + C::COL_S, c0, lse2_a, lse2_b, p.scale_log2e, (d.flags & kDiag) != 0, row, P);
             prof_add(c, kRoleSoftmax, 8, tc0);
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(BAR(B_P_READY));
-            if (warp == 8 && lane == 0) trace_ev<kProf>(p, pp, EV_SM_P_DONE);
+            if (rec) trace_ev<kProf>(p, pp, EV_SM_P_DONE);
             if (!waitw(BAR(B_DP_FULL), (uint32_t)(pp & 1), c, kRoleSoftmax, (int)pp, 2)) break;
-            if (warp == 8 && lane == 0) trace_ev<kProf>(p, pp, EV_SM_DP_SEEN);
+            if (rec) trace_ev<kProf>(p, pp, EV_SM_DP_SEEN);
             ptx::tc_fence_after();
-            uint32_t pk[32];
+            if (pp > 0 && !waitw(BAR(B_DS_FREE), (uint32_t)((pp - 1) & 1), c, kRoleSoftmax, (int)pp, 3)) break;
             tc0 = kProf ? clock64() : 0ull;
-            ds_64(tmem + lane_off + C::COL_DP, c0, vec + 128, p.scale, P, pk);
+            ds_64(tmem + lane_off + C::COL_DP, c0, delta_a, delta_b, p.scale, P, ds_box, row);
             prof_add(c, kRoleSoftmax, 9, tc0);
             ptx::tc_fence_before();
-            if (pp > 0 && !waitw(BAR(B_DS_FREE), (uint32_t)((pp - 1) & 1), c, kRoleSoftmax, (int)pp, 3)) break;
-            store_row_sw128(ds_box, row, pk);
             ptx::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                ptx::mbar_arrive(BAR(B_DS_READY));
-                ptx::mbar_arrive(BAR(B_Q_EMPTY + st));
-            }
-            if (warp == 8 && lane == 0) trace_ev<kProf>(p, pp, EV_SM_DS_DONE);
+            if (lane == 0) ptx::mbar_arrive(BAR(B_DS_READY));
+            if (rec) trace_ev<kProf>(p, pp, EV_SM_DS_DONE);
         }
-    } else if (warp < 4) {
-        // ================================================== dQ drain + dK/dV epilogue
-        const int row = 32 * warp + lane;
-        const uint32_t lane_off = (uint32_t)(32 * warp) << 16;
-        uint8_t* stg = smem + C::OFF_STG;
+    } else {
+        ptx::setmaxnreg_dec<Regs<D>::kDrain>();
+        // ================================================== dQ drain + ordered reduction + dK/dV epilogue
+        const int sub = warp & 3;
+        const int half = (wg == 4) ? 1 : 0;
+        const int st = 2 * sub + half;                     // dQ sub-tile: rows 16*st .. 16*st+15
+        const uint32_t q_lanes = (uint32_t)(32 * sub + 16 * half) << 16;
+        const uint32_t kv_lanes = (uint32_t)(32 * sub) << 16;
+        const int qa = 16 * st + (lane >> 2);              // rows of this lane's fragments: qa, qa + 8
+        const int ca = 2 * (lane & 3);                     // column of the first fragment element
+        const bool odd = lane & 1;
+        const bool rec = warp == 4 && lane == 0;
         int kvc = 0;
-        long long u = 0;   // staging-buffer uses
         for (long long pp = 0;; ++pp) {
             const int ds = (int)(pp % kNDesc);
-            if (!waitw(BAR(B_DESC_FULL + ds), (uint32_t)((pp / kNDesc) & 1), c, kRoleReducer, (int)pp, 0)) break;
+            if (!waitw(BAR(B_DESC_FULL + ds), (uint32_t)((pp / kNDesc) & 1), c, kRoleDrain, (int)pp, 0)) break;
             const PairDesc d = descs[ds];
             if (d.flags & kEnd) break;
-            if (!waitw(BAR(B_DQ_FULL), (uint32_t)(pp & 1), c, kRoleReducer, (int)pp, 1)) break;
-            if (warp == 0 && lane == 0) trace_ev<kProf>(p, pp, EV_DR_DQ_SEEN);
+            if (!waitw(BAR(B_DQ_FULL), (uint32_t)(pp & 1), c, kRoleDrain, (int)pp, 1)) break;
+            if (rec) trace_ev<kProf>(p, pp, EV_DR_DQ_SEEN);
             ptx::tc_fence_after();
-            const int tile = (d.b * p.Hq + d.hq) * p.n + d.q;
-            float* gpart = p.partials ? p.partials + (((size_t)tile * p.n + d.kv) * 128 + row) * D : nullptr;
-            bool ok = true;
-#pragma unroll 1
-            for (int h = 0; h < C::kHalves; ++h) {
-                uint32_t r0[32], r1[32];
-                ptx::tmem_ld32(tmem + lane_off + C::COL_DQ + 64 * h, r0);
-                ptx::tmem_ld32(tmem + lane_off + C::COL_DQ + 64 * h + 32, r1);
-                ptx::tmem_ld_wait();
-                if (h == C::kHalves - 1) {   // dQ columns go back to the MMA issuer
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(BAR(B_DQ_EMPTY));
-                    if (warp == 0 && lane == 0) trace_ev<kProf>(p, pp, EV_DR_DQ_EMPTY);
-                }
-                if (gpart) {
+            // Read the sub-tile (16 rows x D) out of tensor memory, then hand the
+            // columns back to the MMA issuer.
+            uint32_t r[D / 2];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        *reinterpret_cast<uint4*>(gpart + 64 * h + 4 * e) =
-                            make_uint4(r0[4 * e], r0[4 * e + 1], r0[4 * e + 2], r0[4 * e + 3]);
-                        *reinterpret_cast<uint4*>(gpart + 64 * h + 32 + 4 * e) =
-                            make_uint4(r1[4 * e], r1[4 * e + 1], r1[4 * e + 2], r1[4 * e + 3]);
+            for (int b = 0; b < D / 64; ++b)
+                ptx::tmem_ld16x256_x8(tmem + q_lanes + C::COL_DQ + 64 * b,
+                                      *reinterpret_cast<uint32_t(*)[32]>(&r[32 * b]));
+            ptx::tmem_ld_wait();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(BAR(B_DQ_EMPTY));
+            if (rec) trace_ev<kProf>(p, pp, EV_DR_DQ_EMPTY);
+            const int tile = (d.b * p.Hq + d.hq) * p.n + d.q;
+            if (p.partials) {
+                float* gp = p.partials + ((size_t)tile * p.n + d.kv) * 128 * D;
+#pragma unroll
+                for (int j = 0; j < D / 8; ++j) {
+                    *reinterpret_cast<float2*>(gp + (size_t)qa * D + 8 * j + ca) =
+                        make_float2(__uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]));
+                    *reinterpret_cast<float2*>(gp + (size_t)(qa + 8) * D + 8 * j + ca) =
+                        make_float2(__uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                }
+            }
+            // Pair exchange inside each lane quad: afterwards a lane holds 4
+            // consecutive columns of one 8-column chunk (even lanes: chunk j,
+            // odd lanes: chunk j+1) for its two rows.
+#pragma unroll
+            for (int j = 0; j < D / 8; j += 2) {
+                const uint32_t s0 = odd ? r[4 * j] : r[4 * (j + 1)];
+                const uint32_t s1 = odd ? r[4 * j + 1] : r[4 * (j + 1) + 1];
+                const uint32_t s2 = odd ? r[4 * j + 2] : r[4 * (j + 1) + 2];
+                const uint32_t s3 = odd ? r[4 * j + 3] : r[4 * (j + 1) + 3];
+                const uint32_t g0 = __shfl_xor_sync(0xffffffffu, s0, 1);
+                const uint32_t g1 = __shfl_xor_sync(0xffffffffu, s1, 1);
+                const uint32_t g2 = __shfl_xor_sync(0xffffffffu, s2, 1);
+                const uint32_t g3 = __shfl_xor_sync(0xffffffffu, s3, 1);
+                if (odd) {   // keeps chunk j+1: partner's lower pair first
+                    r[4 * j] = g0;
+                    r[4 * j + 1] = g1;
+                    r[4 * j + 2] = r[4 * (j + 1)];
+                    r[4 * j + 3] = r[4 * (j + 1) + 1];
+                    const uint32_t b2 = r[4 * (j + 1) + 2], b3 = r[4 * (j + 1) + 3];
+                    r[4 * (j + 1)] = g2;
+                    r[4 * (j + 1) + 1] = g3;
+                    r[4 * (j + 1) + 2] = b2;
+                    r[4 * (j + 1) + 3] = b3;
+                } else {     // keeps chunk j: own pair first
+                    const uint32_t a2 = r[4 * j + 2], a3 = r[4 * j + 3];
+                    r[4 * j + 2] = g0;
+                    r[4 * j + 3] = g1;
+                    r[4 * (j + 1)] = a2;
+                    r[4 * (j + 1) + 1] = a3;
+                    r[4 * (j + 1) + 2] = g2;
+                    r[4 * (j + 1) + 3] = g3;
+                }
+            }
+            // this lane now holds, for chunk pair (j, j+1): row qa cols cb..cb+3 in
+            // r[4j..4j+3] and row qa+8 cols cb..cb+3 in r[4(j+1)..4(j+1)+3],
+            // cb = 8*(j + odd) + 2*(lane & 2)
+            bool ok = true;
+            if (ordered) {
+                int* sem = p.sem + (size_t)tile * kSubTiles + st;
+                int good = 1;
+                if (lane == 0) {
+                    const unsigned long long t0 = kProf ? clock64() : 0ull;
+                    good = wait_turn(p, c, abort_smem, sem, d.rank, d.b * p.Hq + d.hq, tile % p.n) ? 1 : 0;
+                    prof_add(c, kRoleDrain, 8, t0);
+                    if (good && st == 0 && p.order_log) {
+                        const int s = atomicAdd(p.logcnt + tile, 1);
+                        if (s >= 0 && s < p.n) p.order_log[(size_t)tile * p.n + s] = d.kv;
                     }
                 }
-                const unsigned long long t0 = kProf ? clock64() : 0ull;
-                if (u > 0 && !waitw(BAR(B_STG_EMPTY), (uint32_t)((u - 1) & 1), c, kRoleReducer, (int)pp, 3)) {
-                    ok = false;
-                    break;
-                }
-                store_row_f32_sw128(stg, row, r0);
-                store_row_f32_sw128(stg + kBox, row, r1);
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(BAR(B_STG_FULL));
-                if (warp == 0 && lane == 0) trace_ev<kProf>(p, pp, EV_DR_STAGED0 + (h & 1));
-                prof_add(c, kRoleReducer, 8, t0);
-                ++u;
+                ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+            } else if (st == 0 && p.order_log && lane == 0) {
+                const int s = atomicAdd(p.logcnt + tile, 1);
+                if (s >= 0 && s < p.n) p.order_log[(size_t)tile * p.n + s] = d.kv;
             }
             if (!ok) break;
+            if (rec) trace_ev<kProf>(p, pp, EV_DR_TURN);
+            float* gdq = p.dq + ((size_t)(d.b * p.Hq + d.hq) * p.S + (size_t)d.q * 128) * D;
+            const int cofs = 2 * (lane & 2);
+#pragma unroll
+            for (int j = 0; j < D / 8; j += 2) {
+                const int cb = 8 * (j + (odd ? 1 : 0)) + cofs;
+                ptx::red_add_v4(gdq + (size_t)qa * D + cb, __uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                ptx::red_add_v4(gdq + (size_t)(qa + 8) * D + cb, __uint_as_float(r[4 * (j + 1)]),
+                                __uint_as_float(r[4 * (j + 1) + 1]), __uint_as_float(r[4 * (j + 1) + 2]),
+                                __uint_as_float(r[4 * (j + 1) + 3]));
+            }
+            if (rec) trace_ev<kProf>(p, pp, EV_DR_REDS);
+            if (ordered) {
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) ptx::st_release(p.sem + (size_t)tile * kSubTiles + st, d.rank + 1);
+            }
+            if (rec) trace_ev<kProf>(p, pp, EV_DR_DONE);
+            if (lane == 0) ptx::mbar_arrive(BAR(B_DESC_EMPTY + ds));
             if (d.flags & kKvLast) {
-                if (!waitw(BAR(B_ACC_FULL), (uint32_t)(kvc & 1), c, kRoleReducer, (int)pp, 2)) break;
+                // dK (drain warps of WG1) and dV (WG4) of the finished KV tile
+                if (!waitw(BAR(B_ACC_FULL), (uint32_t)(kvc & 1), c, kRoleDrain, (int)pp, 2)) break;
                 ptx::tc_fence_after();
-                const size_t grow = ((size_t)(d.b * p.Hkv + d.hkv) * p.S + (size_t)d.kv * 128 + row) * D;
+                const int krow = 32 * sub + lane;
+                const size_t grow = ((size_t)(d.b * p.Hkv + d.hkv) * p.S + (size_t)d.kv * 128 + krow) * D;
+                __nv_bfloat16* out = (half == 0 ? p.dk : p.dv) + grow;
+                const uint32_t col = half == 0 ? C::COL_DK : C::COL_DV;
 #pragma unroll
-                for (int which = 0; which < 2; ++which) {
-                    __nv_bfloat16* out = (which == 0 ? p.dk : p.dv) + grow;
-                    const uint32_t col = which == 0 ? C::COL_DK : C::COL_DV;
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t v[32];
+                    ptx::tmem_ld32(tmem + kv_lanes + col + 32 * cc, v);
+                    ptx::tmem_ld_wait();
+                    uint32_t pk[16];
 #pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t r[32];
-                        ptx::tmem_ld32(tmem + lane_off + col + 32 * cc, r);
-                        ptx::tmem_ld_wait();
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            __nv_bfloat162 h2 =
-                                __floats2bfloat162_rn(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
-                            pk[e] = *reinterpret_cast<uint32_t*>(&h2);
-                        }
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            *reinterpret_cast<uint4*>(out + 32 * cc + 8 * e) =
-                                make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
-                        }
+                    for (int e = 0; e < 16; ++e) {
+                        __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+                        pk[e] = *reinterpret_cast<uint32_t*>(&h2);
                     }
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        *reinterpret_cast<uint4*>(out + 32 * cc + 8 * e) =
+                            make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
                 }
                 ptx::tc_fence_before();
                 __syncwarp();
@@ -583,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
 
     ptx::tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 1) {
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, 512);
     }
@@ -607,6 +610,15 @@ int launch_bwd(const BwdParams& prm, int grid, cudaStream_t stream) {
             return -2;
         attr_done[dev] = true;
     }
+    // The warpgroups re-split the block's registers with setmaxnreg; that is
+    // only safe if the compiled kernel was granted the registers it assumes.
+    static int regs_ok[64] = {};
+    if (dev >= 0 && dev < 64 && regs_ok[dev] == 0) {
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, dash_bwd_kernel<D, kProf>) != cudaSuccess) return -2;
+        regs_ok[dev] = (fa.numRegs >= kRegsLaunch) ? 1 : -1;
+    }
+    if (dev < 0 || dev >= 64 || regs_ok[dev] != 1) return -3;
     void* args[] = {(void*)&prm};
     cudaError_t e = cudaLaunchCooperativeKernel((const void*)dash_bwd_kernel<D, kProf>, dim3(grid),
                                                 dim3(kThreads), args, C::kSmem, stream);

@@ -22,19 +22,23 @@
 // its rank in the schedule's accumulation order (gist.science DASH summary,
 // section 1: a fixed accumulation order makes dQ reproducible).
 //
-// Warp roles (16 warps, 512 threads):
-//   warps 0-3   drain: read dQ out of tensor memory into a swizzled fp32
-//               staging buffer in shared memory, and the dK/dV epilogue of
-//               each KV tile;
-//   warp 4      producer: task dispatch, pair descriptors, TMA loads;
-//   warp 5      MMA issuer (one thread) and TMEM owner;
-//   warp 6      reduce issuer (one thread): waits for the pair's turn, adds
-//               the staged dQ partial into global dq with TMA reduce-add
-//               (cp.reduce.async.bulk.tensor), waits for completion, releases
-//               the turn;
-//   warp 7      idle;
-//   warps 8-15  softmax / dS: warp w owns TMEM lanes 32*(w%4).. and the Q
-//               columns 64*((w-8)/4) .. +63 of the pair.
+// Warp roles (20 warps, 640 threads, five warpgroups):
+//   WG0  warp 0 producer (task dispatch, pair descriptors, TMA loads),
+//        warp 1 MMA issuer (one thread) and TMEM owner, warps 2-3 idle;
+//   WG1  warps 4-7   dQ drain, TMEM lanes 32*(w%4) + 0..15;
+//   WG2  warps 8-11  softmax / dS, Q columns 0..63;
+//   WG3  warps 12-15 softmax / dS, Q columns 64..127;
+//   WG4  warps 16-19 dQ drain, TMEM lanes 32*(w%4) + 16..31.
+// A drain warp owns 16 rows of the dQ tile (a sub-tile): it reads them out
+// of tensor memory (16x256b shape), hands the columns back to the MMA issuer,
+// waits for the pair's turn on its own sub-tile counter and adds its rows
+// into global dq with 64-byte-per-row fp32 vector reductions straight from
+// registers.  Nothing but the tensor core reads shared memory in the steady
+// state: thread loads from shared memory and TMA stores from it are starved
+// while the tensor core streams its operands, so LSE and delta reach the
+// softmax warps through global loads and warp shuffles.  The eight
+// sub-tiles of a dQ tile carry the same accumulation rank, so the order of
+// the additions into every element is the schedule's.
 //
 // Tensor memory (512 columns): dK [0,D), dV [D,2D), S/P [2D, 2D+128),
 // dP [2D+128, 2D+256); dQ aliases dP when D = 128 and has its own 64
@@ -42,8 +46,8 @@
 //
 // Every wait is bounded (%globaltimer); a wait that runs out records the
 // failure in the status word, raises a CTA-wide and a grid-wide abort flag,
-// and every role then leaves its loop; the CTA waits for its own TMA loads,
-// reductions and MMAs to land, frees tensor memory and exits.
+// and every role then leaves its loop; the CTA waits for its own TMA loads
+// and MMAs to land, frees tensor memory and exits.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -54,12 +58,13 @@
 
 namespace dash {
 
-constexpr int kThreads = 512;
+constexpr int kThreads = 640;
+constexpr int kSubTiles = 8;        // dQ sub-tiles (16 rows each) with their own turn counters
 constexpr int kBox = 16384;        // 128 rows x 128 B
 constexpr int kNDesc = 8;          // pair-descriptor ring depth
 constexpr float kLog2e = 1.4426950408889634f;
 
-enum Role : int { kRoleReducer = 0, kRoleProducer = 1, kRoleMma = 2, kRoleSoftmax = 3, kRoleIssuer = 4 };
+enum Role : int { kRoleDrain = 0, kRoleProducer = 1, kRoleMma = 2, kRoleSoftmax = 3 };
 enum DescFlags : int { kKvFirst = 1, kKvLast = 2, kDiag = 4, kEnd = 8 };
 
 // Barrier slots (8 bytes each) at the start of the control area.
@@ -81,25 +86,22 @@ enum Bar : int {
     B_DQ_EMPTY,
     B_ACC_FULL,
     B_ACC_EMPTY,
-    B_STG_FULL,
-    B_STG_EMPTY,
     B_DRAIN,
     B_COUNT
 };
 
 // Control area: barriers [0, 320), descriptors [320, 576), TMEM address
-// 576, abort flag 580, cycle counters [584, 992).
+// 576, abort flag 580, cycle counters [584, ...).
 constexpr int kCtlBars = 0, kCtlDescs = 320, kCtlTmem = 576, kCtlAbort = 580, kCtlProf = 584;
 constexpr int kProfPerRole = 10;
-constexpr int kProfSmem = 5 * kProfPerRole + 1;   // + whole-CTA cycles
+constexpr int kProfSmem = 4 * kProfPerRole + 1;   // + whole-CTA cycles
 constexpr int kProfOut = 64;                       // per-CTA entries in the debug buffer
 constexpr int kTracePairs = 64;                    // event trace of the first pairs of CTA 0
 constexpr int kTraceEvents = 32;
 enum TraceEv : int {
     EV_S_ISSUE = 0, EV_DP_ISSUE, EV_DV_ISSUE, EV_DK_ISSUE, EV_DQ_ISSUE,         // MMA issuer
     EV_SM_S_SEEN = 5, EV_SM_P_DONE, EV_SM_DP_SEEN, EV_SM_DS_DONE,               // softmax warp 8
-    EV_DR_DQ_SEEN = 10, EV_DR_DQ_EMPTY, EV_DR_STAGED0, EV_DR_STAGED1,           // drain warp 0
-    EV_IS_STG_SEEN = 15, EV_IS_TURN, EV_IS_READ0, EV_IS_READ1, EV_IS_DONE,      // reduce issuer
+    EV_DR_DQ_SEEN = 10, EV_DR_DQ_EMPTY, EV_DR_TURN, EV_DR_REDS, EV_DR_DONE,     // drain warp 4
     EV_PR_DESC = 22, EV_PR_Q_ISSUED, EV_PR_DO_ISSUED                            // producer
 };
 static_assert(B_COUNT * 8 <= kCtlDescs, "barrier area");
@@ -115,16 +117,13 @@ struct Cfg {
     static constexpr int kTile = D * 128 * 2;         // 128 x D bf16
     static constexpr int kNBox = D / 64;
     static constexpr int kQStages = 2;
-    static constexpr int kDoStages = (D == 128) ? 1 : 2;   // dO's last use (dV) comes early
-    static constexpr int kHalves = D / 64;             // staging passes per dQ tile (64 fp32 columns each)
+    static constexpr int kDoStages = 2;
     static constexpr int OFF_K = 0;
     static constexpr int OFF_V = OFF_K + kTile;
     static constexpr int OFF_Q = OFF_V + kTile;
     static constexpr int OFF_DO = OFF_Q + kQStages * kTile;
     static constexpr int OFF_DS = OFF_DO + kDoStages * kTile;
-    static constexpr int OFF_STG = OFF_DS + 2 * kBox;  // fp32 staging: 2 boxes of 128 rows x 32 floats
-    static constexpr int OFF_VEC = OFF_STG + 2 * kBox; // per Q stage: LSE[128], delta[128]
-    static constexpr int OFF_CTL = OFF_VEC + kQStages * 1024;
+    static constexpr int OFF_CTL = OFF_DS + 2 * kBox;
     static constexpr int kSmem = OFF_CTL + 1024;
     static constexpr uint32_t COL_DK = 0;
     static constexpr uint32_t COL_DV = D;
@@ -132,23 +131,33 @@ struct Cfg {
     static constexpr uint32_t COL_DP = 2 * D + 128;
     static constexpr bool kDqAlias = (D == 128);
     static constexpr uint32_t COL_DQ = kDqAlias ? COL_DP : 2 * D + 256;
-    static constexpr uint32_t kQBytes = kTile + 1024;   // Q tile + LSE + delta
+    static constexpr uint32_t kQBytes = kTile;
     static constexpr uint32_t kDoBytes = kTile;
     static constexpr uint32_t kKvBytes = 2 * kTile;
     static_assert(kSmem <= 232448, "shared memory budget");
     static_assert(COL_DQ + D <= 512, "tensor memory budget");
 };
 
+// Register split of the five warpgroups (setmaxnreg); the launch must grant
+// kRegsLaunch registers per thread so that the split fits the block's pool.
+constexpr int kRegsLaunch = 96;
+template <int D>
+struct Regs {
+    static constexpr int kCtl = 64;
+    static constexpr int kDrain = (D == 128) ? 88 : 80;
+    static constexpr int kSoftmax = (D == 128) ? 112 : 120;
+    static_assert(128 * kCtl + 256 * kDrain + 256 * kSoftmax <= kThreads * kRegsLaunch, "register split");
+};
+
 struct BwdParams {
     CUtensorMap tm_q, tm_k, tm_v, tm_do;   // 2D [rows, D] bf16, box 64 x 128, SWIZZLE_128B
-    CUtensorMap tm_dq;                      // 2D [rows, D] fp32, box 32 x 128, SWIZZLE_128B
     const float* lse;
     const float* delta;
     float* dq;
     __nv_bfloat16* dk;
     __nv_bfloat16* dv;
     const uint16_t* ranks;                  // static schedules: [B*Hq*n][n]
-    int* sem;                               // [B*Hq*n] accumulation counters
+    int* sem;                               // [B*Hq*n][kSubTiles] accumulation counters
     int* logcnt;                            // [B*Hq*n] order-log cursors
     int* task_counter;                      // dynamic dispatch
     int* status;                            // [8]: code, info[4]
@@ -218,67 +227,69 @@ __device__ __forceinline__ void issue_dq(uint32_t d_tmem, uint32_t sDsT, uint32_
 
 // ------------------------------------------------------------ softmax / dS
 // Executed by one warp that owns TMEM lanes [lane_base, lane_base+32) (KV rows)
-// and Q columns [c0, c0+64) of the pair.
+// and Q columns [c0, c0+64) of the pair.  Lane l holds the per-column
+// statistics of columns c0 + l (x_a) and c0 + 32 + l (x_b); column k's value
+// reaches every lane through a shuffle.
 
 // P for 64 columns: reads S^T, writes P (fp32, registers) and the packed
-// bf16 P^T back into tensor memory at columns [col_s + c0/2 .. ) of its own
-// 64-column span (so the MMA reads it as a K-major A operand).
-__device__ __forceinline__ void softmax_64(uint32_t tmem_s_lane, int c0, const float* lse,
+// bf16 P^T back into tensor memory at columns [c0, c0+32) of its own
+// 64-column span (so the MMA reads it as a K-major A operand).  lse2_* are
+// LSE * log2(e).  Works in 32-column halves to keep few registers live.
+__device__ __forceinline__ void softmax_64(uint32_t tmem_s_lane, int c0, float lse2_a, float lse2_b,
                                            float scale_log2e, bool diag, int row, float (&P)[64]) {
-    uint32_t r0[32], r1[32];
-    ptx::tmem_ld32(tmem_s_lane + c0, r0);
-    ptx::tmem_ld32(tmem_s_lane + c0 + 32, r1);
-    ptx::tmem_ld_wait();
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-        const int q = c0 + k;
-        float x = ptx::ex2(fmaf(__uint_as_float(r0[k]), scale_log2e, -lse[q] * kLog2e));
-        P[k] = (diag && row > q) ? 0.f : x;
-    }
+    for (int h = 0; h < 2; ++h) {
+        uint32_t r[32];
+        ptx::tmem_ld32(tmem_s_lane + c0 + 32 * h, r);
+        ptx::tmem_ld_wait();
+        const float lsrc = h ? lse2_b : lse2_a;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-        const int q = c0 + 32 + k;
-        float x = ptx::ex2(fmaf(__uint_as_float(r1[k]), scale_log2e, -lse[q] * kLog2e));
-        P[32 + k] = (diag && row > q) ? 0.f : x;
-    }
-    uint32_t pk[32];
+        for (int k = 0; k < 32; ++k) {
+            const float l = __shfl_sync(0xffffffffu, lsrc, k);
+            const float x = ptx::ex2(fmaf(__uint_as_float(r[k]), scale_log2e, -l));
+            P[32 * h + k] = (diag && row > c0 + 32 * h + k) ? 0.f : x;
+        }
+        uint32_t pk[16];
 #pragma unroll
-    for (int k = 0; k < 32; ++k) {
-        __nv_bfloat162 h2 = __floats2bfloat162_rn(P[2 * k], P[2 * k + 1]);
-        pk[k] = *reinterpret_cast<uint32_t*>(&h2);
+        for (int k = 0; k < 16; ++k) {
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(P[32 * h + 2 * k], P[32 * h + 2 * k + 1]);
+            pk[k] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+        // packed columns [c0 + 16h, c0 + 16h + 16): S values there were already read
+        ptx::tmem_st16(tmem_s_lane + c0 + 16 * h, pk);
     }
-    ptx::tmem_st32(tmem_s_lane + c0, pk);
     ptx::tmem_st_wait();
 }
 
-// dS^T = scale * P o (dP^T - delta) for 64 columns; the bf16 result goes to
-// the K-major swizzled box `box_saddr` (row `row`), i.e. box c0/64 of dS^T.
-__device__ __forceinline__ void ds_64(uint32_t tmem_dp_lane, int c0, const float* delta, float scale,
-                                      const float (&P)[64], uint32_t pk[32]) {
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-        uint32_t r[32];
-        ptx::tmem_ld32(tmem_dp_lane + c0 + 32 * half, r);
-        ptx::tmem_ld_wait();
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            const int a = 32 * half + 2 * k;
-            const float d0 = P[a] * (__uint_as_float(r[2 * k]) - delta[c0 + a]) * scale;
-            const float d1 = P[a + 1] * (__uint_as_float(r[2 * k + 1]) - delta[c0 + a + 1]) * scale;
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(d0, d1);
-            pk[16 * half + k] = *reinterpret_cast<uint32_t*>(&h2);
-        }
-    }
-}
-
-// 32 fp32 values of one row into a 128-byte-swizzled fp32 box (128 rows x
-// 32 floats): chunk c of 4 floats lands at (c ^ (row % 8)) in the row.
-__device__ __forceinline__ void store_row_f32_sw128(uint8_t* box, int row, const uint32_t (&r)[32]) {
+// dS^T = scale * P o (dP^T - delta) for 64 columns, written as bf16 into row
+// `row` of the K-major swizzled box `box` (box c0/64 of dS^T), 16 columns
+// (two 16-byte chunks) at a time.
+__device__ __forceinline__ void ds_64(uint32_t tmem_dp_lane, int c0, float delta_a, float delta_b, float scale,
+                                      const float (&P)[64], uint8_t* box, int row) {
     uint8_t* rp = box + row * 128;
 #pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        uint4 v = make_uint4(r[4 * c], r[4 * c + 1], r[4 * c + 2], r[4 * c + 3]);
-        *reinterpret_cast<uint4*>(rp + ((c ^ (row & 7)) << 4)) = v;
+    for (int q4 = 0; q4 < 4; ++q4) {
+        uint32_t r[16];
+        ptx::tmem_ld16(tmem_dp_lane + c0 + 16 * q4, r);
+        ptx::tmem_ld_wait();
+        const float dsrc = (q4 < 2) ? delta_a : delta_b;
+        uint32_t pk[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int a = 16 * q4 + 2 * k;
+            const float e0 = __shfl_sync(0xffffffffu, dsrc, (a & 31));
+            const float e1 = __shfl_sync(0xffffffffu, dsrc, (a & 31) + 1);
+            const float d0 = P[a] * (__uint_as_float(r[2 * k]) - e0) * scale;
+            const float d1 = P[a + 1] * (__uint_as_float(r[2 * k + 1]) - e1) * scale;
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(d0, d1);
+            pk[k] = *reinterpret_cast<uint32_t*>(&h2);
+        }
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            const int chunk = 2 * q4 + c;   // 16-byte chunk (8 columns) within the 128-byte row
+            *reinterpret_cast<uint4*>(rp + ((chunk ^ (row & 7)) << 4)) =
+                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
     }
 }
 

@@ -43,7 +43,6 @@ __global__ void __launch_bounds__(256, 1) probe_kernel(const __grid_constant__ P
     // layout: K, V, Q, dO tiles, dS^T (2 boxes), LSE/delta, barriers
     const uint32_t sbase = ptx::smem_u32(smem);
     const uint32_t sK = sbase, sV = sbase + T, sQ = sbase + 2 * T, sDO = sbase + 3 * T, sDS = sbase + 4 * T;
-    float* vec = reinterpret_cast<float*>(smem + 4 * T + 2 * kBox);
     uint8_t* ctl = smem + 4 * T + 2 * kBox + 1024;
     const uint32_t bar_tma = ptx::smem_u32(ctl), bar_mma = bar_tma + 8;
     volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(ctl + 64);
@@ -67,15 +66,13 @@ __global__ void __launch_bounds__(256, 1) probe_kernel(const __grid_constant__ P
     const uint32_t tmem = *tmem_slot;
     bool ok = *bad == 0;
     if (ok && threadIdx.x == 0) {
-        ptx::mbar_arrive_expect_tx(bar_tma, 4 * T + 1024);
+        ptx::mbar_arrive_expect_tx(bar_tma, 4 * T);
         for (int bx = 0; bx < C::kNBox; ++bx) {
             ptx::tma_load_2d(sK + bx * kBox, &p.tm_k, 64 * bx, 0, bar_tma);
             ptx::tma_load_2d(sV + bx * kBox, &p.tm_v, 64 * bx, 0, bar_tma);
             ptx::tma_load_2d(sQ + bx * kBox, &p.tm_q, 64 * bx, 0, bar_tma);
             ptx::tma_load_2d(sDO + bx * kBox, &p.tm_do, 64 * bx, 0, bar_tma);
         }
-        ptx::bulk_load(ptx::smem_u32(vec), p.lse, 512, bar_tma);
-        ptx::bulk_load(ptx::smem_u32(vec + 128), p.delta, 512, bar_tma);
     }
     if (ok) ok = probe_wait(bar_tma, 0, p.err);
     ok = __syncthreads_and(ok);
@@ -90,6 +87,8 @@ __global__ void __launch_bounds__(256, 1) probe_kernel(const __grid_constant__ P
 
     const int sub = warp & 3, c0 = 64 * (warp >> 2), row = 32 * sub + lane;
     const uint32_t lane_off = (uint32_t)(32 * sub) << 16;
+    const float lse2_a = p.lse[c0 + lane] * kLog2e, lse2_b = p.lse[c0 + 32 + lane] * kLog2e;
+    const float delta_a = p.delta[c0 + lane], delta_b = p.delta[c0 + 32 + lane];
     float P[64];
     if (ok) {
         ptx::tc_fence_after();
@@ -99,7 +98,7 @@ __global__ void __launch_bounds__(256, 1) probe_kernel(const __grid_constant__ P
             ptx::tmem_ld_wait();
             for (int k = 0; k < 32; ++k) p.sT[row * 128 + c0 + 32 * h + k] = __uint_as_float(r[k]);
         }
-        softmax_64(tmem + lane_off + C::COL_S, c0, vec, p.scale_log2e, p.diag != 0, row, P);
+        softmax_64(tmem + lane_off + C::COL_S, c0, lse2_a, lse2_b, p.scale_log2e, p.diag != 0, row, P);
         for (int k = 0; k < 64; ++k) p.pT[row * 128 + c0 + k] = P[k];
         ptx::tc_fence_before();
     }
@@ -119,17 +118,20 @@ __global__ void __launch_bounds__(256, 1) probe_kernel(const __grid_constant__ P
             ptx::tmem_ld_wait();
             for (int k = 0; k < 32; ++k) p.dpT[row * 128 + c0 + 32 * h + k] = __uint_as_float(r[k]);
         }
-        uint32_t pk[32];
-        ds_64(tmem + lane_off + C::COL_DP, c0, vec + 128, p.scale, P, pk);
-        for (int k = 0; k < 32; ++k) {
-            const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(&pk[k]);
-            const float2 f = __bfloat1622float2(h2);
-            p.dsT[row * 128 + c0 + 2 * k] = f.x;
-            p.dsT[row * 128 + c0 + 2 * k + 1] = f.y;
-        }
+        uint8_t* box = smem + 4 * T + (c0 >> 6) * kBox;
+        ds_64(tmem + lane_off + C::COL_DP, c0, delta_a, delta_b, p.scale, P, box, row);
         ptx::tc_fence_before();
-        store_row_sw128(smem + 4 * T + (c0 >> 6) * kBox, row, pk);
         ptx::fence_proxy_async_smem();
+        // read the bf16 dS^T row back (unswizzled) for the dump
+        for (int cc = 0; cc < 8; ++cc) {
+            const uint4 v4 = *reinterpret_cast<const uint4*>(box + row * 128 + ((cc ^ (row & 7)) << 4));
+            const uint32_t w4[4] = {v4.x, v4.y, v4.z, v4.w};
+            for (int e = 0; e < 4; ++e) {
+                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w4[e]));
+                p.dsT[row * 128 + c0 + 8 * cc + 2 * e] = f.x;
+                p.dsT[row * 128 + c0 + 8 * cc + 2 * e + 1] = f.y;
+            }
+        }
     }
     ok = __syncthreads_and(ok);
     if (ok && threadIdx.x == 0) {
