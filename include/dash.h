@@ -50,7 +50,8 @@ typedef enum {
     DASH_ERR_TIMEOUT = -4,    /* device-side wait exceeded the timeout (reported by dash_get_status) */
     DASH_ERR_DEADLOCK = -5,   /* a schedule table cannot complete (cycle or missing predecessor) */
     DASH_ERR_NOMEM = -6,      /* workspace allocation failed */
-    DASH_ERR_DEVICE = -7      /* device is not sm_103 / lacks the needed shared memory */
+    DASH_ERR_DEVICE = -7,     /* device is not sm_103 / lacks the needed shared memory */
+    DASH_ERR_SCRATCH = -8     /* problem needs more than dash_attn_bwd_noalloc's fixed scratch */
 } dash_status;
 
 typedef enum {
@@ -106,6 +107,38 @@ int dash_attn_bwd(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v,
                   float* dq, dash_bf16* dk, dash_bf16* dv,
                   int B, int Hq, int Hkv, int S, int D, int causal, int schedule,
                   dash_stream_t stream);
+
+/*
+ * dash_attn_bwd_noalloc -- dash_attn_bwd for callers that cannot allocate.
+ *
+ * No counterpart on the DASH pages: this is a deployment variant.  Same
+ * arguments, outputs, determinism and errors as dash_attn_bwd, but it never
+ * calls cudaMalloc/cudaFree or any allocating routine.  It is meant for
+ * callers that have given all device memory to their own pool allocator, or
+ * that run on a latency-critical path where the implicit synchronization of
+ * cudaMalloc/cudaFree is not acceptable.  The caller still provides every
+ * input and output buffer.
+ *
+ * Scratch (delta, the accumulation counters, the rank tables) comes from one
+ * 8 MiB file-scope device array that every GPU loading the library keeps
+ * until the process exits.  A problem needing more returns
+ * DASH_ERR_SCRATCH (roughly: B*Hq*S*4 bytes of delta plus, for the shift
+ * schedules, B*Hq*(S/128)^2*6 bytes of tables must fit).
+ *
+ * The first call on a device looks up that device's address of the array
+ * (with the device current); make that first call before any stream
+ * capture.  All calls share the array and it keeps the previous call's
+ * contents: each call clears what must start at zero on its stream, so
+ * calls must not overlap on the GPU (different streams or host threads
+ * racing on the array give undefined results).  A device-side wait that
+ * times out leaves the outputs undefined; this entry point does not report
+ * it through dash_get_status.
+ */
+int dash_attn_bwd_noalloc(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v,
+                          const dash_bf16* o, const dash_bf16* dO, const float* lse,
+                          float* dq, dash_bf16* dk, dash_bf16* dv,
+                          int B, int Hq, int Hkv, int S, int D, int causal, int schedule,
+                          dash_stream_t stream);
 
 /*
  * dash_dq_finalize -- dq[i] = bf16_round_to_nearest_even(dq_accum[i]) for

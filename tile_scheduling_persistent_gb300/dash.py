@@ -18,13 +18,14 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libdash.so")
 
 OK, ERR_ARG, ERR_CUDA, ERR_LAUNCH, ERR_TIMEOUT, ERR_DEADLOCK, ERR_NOMEM, ERR_DEVICE = 0, -1, -2, -3, -4, -5, -6, -7
+ERR_SCRATCH = -8
 _NAMES = {0: "DASH_OK", -1: "DASH_ERR_ARG", -2: "DASH_ERR_CUDA", -3: "DASH_ERR_LAUNCH", -4: "DASH_ERR_TIMEOUT",
-          -5: "DASH_ERR_DEADLOCK", -6: "DASH_ERR_NOMEM", -7: "DASH_ERR_DEVICE"}
+          -5: "DASH_ERR_DEADLOCK", -6: "DASH_ERR_NOMEM", -7: "DASH_ERR_DEVICE", -8: "DASH_ERR_SCRATCH"}
 
 EXPORTS = (
     "dash_attn_bwd_preprocess", "dash_attn_bwd", "dash_dq_finalize", "dash_get_status", "dash_set_timeout_ns",
     "dash_release_workspaces", "dash_num_ctas", "dash_sim_schedule", "dash_sim_check_ranks",
-    "dash_attn_bwd_debug", "dash_debug_tile_probe",
+    "dash_attn_bwd_debug", "dash_debug_tile_probe", "dash_attn_bwd_noalloc",
 )
 
 
@@ -57,6 +58,7 @@ def lib():
     L.dash_attn_bwd_preprocess.argtypes = [P, P, P, I, I, I, I, P]
     L.dash_attn_bwd.argtypes = [P] * 9 + [I] * 7 + [P]
     L.dash_attn_bwd_debug.argtypes = [P] * 9 + [I] * 7 + [P, ctypes.POINTER(_DebugOpts)]
+    L.dash_attn_bwd_noalloc.argtypes = [P] * 9 + [I] * 7 + [P]
     L.dash_dq_finalize.argtypes = [P, P, Z, P]
     L.dash_get_status.argtypes = [P, ctypes.POINTER(I), ctypes.POINTER(I)]
     L.dash_set_timeout_ns.argtypes = [ctypes.c_uint64]
@@ -114,6 +116,13 @@ def attn_bwd(q, k, v, o, do, lse, dq, dk, dv, causal, schedule, stream=None):
     """dq (fp32 accumulator, zeroed by the library), dk, dv (bf16) <- backward."""
     _check(lib().dash_attn_bwd(*_bwd_args(q, k, v, o, do, lse, dq, dk, dv, causal, schedule), _stream(stream)),
            "dash_attn_bwd")
+
+
+def attn_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, causal, schedule, stream=None):
+    """attn_bwd for callers that cannot allocate: library scratch comes from a
+    fixed device array (see dash_attn_bwd_noalloc in include/dash.h)."""
+    _check(lib().dash_attn_bwd_noalloc(*_bwd_args(q, k, v, o, do, lse, dq, dk, dv, causal, schedule),
+                                       _stream(stream)), "dash_attn_bwd_noalloc")
 
 
 def attn_bwd_debug(q, k, v, o, do, lse, dq, dk, dv, causal, schedule, stream=None, order_log=None,
