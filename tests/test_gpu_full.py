@@ -35,10 +35,17 @@ def sampled_groups(w):
     return [(0, 0), (w.B - 1, w.Hkv - 1)]
 
 
-def sample_rows(S, seed):
-    rng = np.random.default_rng(seed)
-    fixed = [0, 1, 127, 128, S // 2, S - 129, S - 128, S - 1]
-    return sorted(set(fixed + list(rng.integers(0, S, 4))))
+def random_rows(S, seed, k=48):
+    """Uniformly drawn rows: their rel-L2 estimates the whole-tensor metric
+    (rows near a causal diagonal have few keys and a larger relative error,
+    so a sample weighted towards them would overstate it)."""
+    return sorted(set(np.random.default_rng(seed).integers(0, S, k).tolist()))
+
+
+def edge_rows(S):
+    """Tile and sequence edges: checked element-wise against the max-abs
+    bound, which holds for any subset of rows."""
+    return [0, 1, 127, 128, S // 2, S - 129, S - 128, S - 1]
 
 
 def setup(name):
@@ -106,12 +113,20 @@ def test_full_size(name):
         for (b, hk), (o_ex, lse_ex) in exact.items():
             heads = list(range(hk * G, (hk + 1) * G))
             qs, ks, vs, dos = q[b:b + 1, heads], k[b:b + 1, hk:hk + 1], v[b:b + 1, hk:hk + 1], do[b:b + 1, heads]
-            rows = sample_rows(w.S, seed=b * 1000 + hk)
+            rnd, edge = random_rows(w.S, seed=b * 1000 + hk), edge_rows(w.S)
+            rows, nr = rnd + edge, len(rnd)
+            got_q, ref_q = [], []
             for gi, hq in enumerate(heads):
                 ref = A.dq_rows(qs, ks, vs, o_ex, dos, lse_ex, w.causal, 0, gi, rows)
-                rel, mx = err(dqb[b, hq, rows], ref)
-                assert rel <= REL_L2 and mx <= MAX_ABS, (sched, "dq", b, hq, rel, mx)
+                g = dqb[b, hq, rows].float().cpu().numpy().astype(np.float64)
+                assert np.abs(g - ref).max() <= MAX_ABS, (sched, "dq max-abs", b, hq)
+                got_q.append(g[:nr])
+                ref_q.append(ref[:nr])
+            rel, _ = err(np.concatenate(got_q), np.concatenate(ref_q))
+            assert rel <= REL_L2, (sched, "dq", b, hk, rel)
             rk, rv = A.dkv_rows(qs, ks, vs, o_ex, dos, lse_ex, w.causal, 0, 0, rows)
             for nm, g, ref in (("dk", dk[b, hk, rows], rk), ("dv", dv[b, hk, rows], rv)):
-                rel, mx = err(g, ref)
-                assert rel <= REL_L2 and mx <= MAX_ABS, (sched, nm, b, hk, rel, mx)
+                g = g.float().cpu().numpy().astype(np.float64)
+                assert np.abs(g - ref).max() <= MAX_ABS, (sched, nm + " max-abs", b, hk)
+                rel, _ = err(g[:nr], ref[:nr])
+                assert rel <= REL_L2, (sched, nm, b, hk, rel)
