@@ -31,6 +31,10 @@ sys.path.insert(0, ROOT)
 
 DEFAULT_WORKLOAD = "full_b4_h16_s4096_d128"
 METRIC = "deterministic attn-bwd TFLOP/s & % of BF16 peak; det/nondet throughput ratio"
+# DRAM bytes (read + write) of one dash_bwd_kernel launch, from one ncu capture
+# (profiles/dash_bwd_kernel_full_b4_h16_s4096_d128_shift.md).  Valid only for
+# the kernel source that capture was taken on: clear it when the kernel changes.
+NCU_TRAFFIC = {("full_b4_h16_s4096_d128", "shift"): 637116672}
 
 
 def parse():
@@ -294,7 +298,8 @@ def main_gpu(args):
         "nondet_tflops": round(world * flop / (ms_nd * 1e-3) / 1e12, 2),
         "schedule_trials_ms": {k: round(v, 4) for k, v in trial.items()},
         "roofline": {"bound": "tensor", "achieved": round(kach, 2), "peak": burst, "unit": "TFLOP/s",
-                     "frac": round(kach / burst, 4), "traffic": None,
+                     "frac": round(kach / burst, 4), "traffic": NCU_TRAFFIC.get((w.name, best)),
+                     "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
                      "kernel": "dash_bwd_kernel", "peak_source": src + " burst bf16 (cuBLAS)",
                      "kernel_ms": round(kms_det, 4), "nondet_kernel_ms": round(kms_nd, 4)},
         "clocks": clocks,
