@@ -304,7 +304,8 @@ def main_gpu(args):
                      "kernel_ms": round(kms_det, 4), "nondet_kernel_ms": round(kms_nd, 4)},
         "clocks": clocks,
         "e2e": {"value": round(world * flop / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e_ms, 4)},
+                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e_ms, 4),
+                "overlap": "double-buffered: copy-in of step k+1 and copy-out of step k-1 overlap step k"},
         "gpu_launches": lps * args.steps,
     }
     if rank == 0 and not args.no_cpu_baseline:
@@ -356,36 +357,65 @@ def wait_profile(w, sched, tensors, outs, warmup, stream, trace_out=None):
 
 
 def e2e_run(w, sched, tensors, steps, warmup, stream):
+    """End to end through the public calls: every step copies its inputs in
+    from pinned host memory, runs the backward + finalize, and copies dQ, dK
+    and dV back to pinned host memory.  Steps are double-buffered over three
+    streams (copy-in, compute, copy-out), so the copy-in of step k+1 and the
+    copy-out of step k-1 overlap the compute of step k, as in a training loop
+    that feeds a stream of independent problems."""
     import torch
     from tile_scheduling_persistent_gb300 import dash
     host = [t.cpu().pin_memory() for t in tensors]
-    dev = [torch.empty_like(t) for t in tensors]
-    dq = torch.empty(w.B, w.Hq, w.S, w.D, dtype=torch.float32, device=dev[0].device)
-    dqb = torch.empty(dq.shape, dtype=torch.bfloat16, device=dq.device)
-    dk = torch.empty(w.B, w.Hkv, w.S, w.D, dtype=torch.bfloat16, device=dq.device)
-    dv = torch.empty_like(dk)
-    out_host = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (dqb, dk, dv)]
+    sets = []
+    for _ in range(2):
+        dev = [torch.empty_like(t) for t in tensors]
+        dq = torch.empty(w.B, w.Hq, w.S, w.D, dtype=torch.float32, device=dev[0].device)
+        dqb = torch.empty(dq.shape, dtype=torch.bfloat16, device=dq.device)
+        dk = torch.empty(w.B, w.Hkv, w.S, w.D, dtype=torch.bfloat16, device=dq.device)
+        dv = torch.empty_like(dk)
+        out_host = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (dqb, dk, dv)]
+        ev = {k: torch.cuda.Event() for k in ("h2d", "comp", "d2h")}
+        sets.append((dev, dq, dqb, dk, dv, out_host, ev))
     h2d = sum(t.numel() * t.element_size() for t in host)
-    d2h = sum(t.numel() * t.element_size() for t in out_host)
+    d2h = sum(t.numel() * t.element_size() for t in sets[0][5])
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    used = [False, False]
 
-    def step():
-        for d, h in zip(dev, host):
-            d.copy_(h, non_blocking=True)
+    def step(i):
+        dev, dq, dqb, dk, dv, out_host, ev = sets[i % 2]
+        with torch.cuda.stream(s_in):
+            if used[i % 2]:
+                s_in.wait_event(ev["comp"])      # step i-2 has finished reading these inputs
+            for d, h in zip(dev, host):
+                d.copy_(h, non_blocking=True)
+            ev["h2d"].record(s_in)
+        stream.wait_event(ev["h2d"])
+        if used[i % 2]:
+            stream.wait_event(ev["d2h"])         # step i-2's outputs have left the device
         q, k, v, o, do, lse = dev
         dash.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, w.causal, sched, stream=stream)
         dash.dq_finalize(dq, dqb, stream=stream)
-        for h, d in zip(out_host, (dqb, dk, dv)):
-            h.copy_(d, non_blocking=True)
+        ev["comp"].record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev["comp"])
+            for h, d in zip(out_host, (dqb, dk, dv)):
+                h.copy_(d, non_blocking=True)
+            ev["d2h"].record(s_out)
+        used[i % 2] = True
 
-    for _ in range(warmup):
-        step()
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(steps):
-        step()
-    b.record(stream)
+    a.record(s_in)
+    for i in range(warmup, warmup + steps):
+        step(i)
+    s_out.wait_event(sets[(warmup + steps - 1) % 2][6]["d2h"])
+    b.record(s_out)
     torch.cuda.synchronize()
+    code, info = dash.get_status(stream)
+    if code != 0:
+        raise RuntimeError("device status %d %s" % (code, info))
     return {"ms": a.elapsed_time(b) / steps, "h2d": h2d, "d2h": d2h}
 
 
