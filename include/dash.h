@@ -59,8 +59,29 @@ typedef enum {
     DASH_SCHED_SERIALIZED_ASCENDING = 1, /* ascending Q visits, ascending-KV accumulation order */
     DASH_SCHED_DESCENDING_Q = 2,         /* descending Q visits, ascending-KV accumulation order */
     DASH_SCHED_SHIFT = 3,                /* cyclic Q rotation per KV tile, model-time order */
-    DASH_SCHED_SYMMETRIC_SHIFT = 4       /* causal: KV pairs (j, n-1-j), two phases; full mask = SHIFT */
+    DASH_SCHED_SYMMETRIC_SHIFT = 4,      /* causal: KV pairs (j, n-1-j), two phases; full mask = SHIFT */
+    DASH_SCHED_AUTO = 5                  /* the deterministic schedule dash_select_schedule picks */
 } dash_schedule;
+
+/*
+ * dash_select_schedule -- the deterministic schedule that DASH_SCHED_AUTO
+ * runs for this shape.  The DASH pages make the choice of strategy a matter
+ * of the hardware: on H800 symmetric shift falls behind descending Q-tile
+ * iteration for causal masks at D = 128 because of register spills
+ * (gist.science summary, section 4), and the pwwt.cn write-up (section 3.1)
+ * switches to descending automatically when head_dim > 64.  On GB300 dK/dV
+ * live in tensor memory and that pressure does not arise; the choice
+ * measured there (152 SMs, kernel-only TFLOP/s) is:
+ *   full mask            -> DASH_SCHED_SHIFT (symmetric shift is the same
+ *                           schedule; ascending is 26% slower)
+ *   causal, D = 128      -> DASH_SCHED_SYMMETRIC_SHIFT (9% ahead of shift,
+ *                           also with grouped-query heads; descending 2x slower)
+ *   causal, D = 64       -> DASH_SCHED_SHIFT (10% ahead of symmetric shift)
+ * A pure function of the shape, never of timing, so that AUTO stays bitwise
+ * reproducible from run to run and process to process.  Returns the
+ * schedule (1..4), or DASH_ERR_ARG for a shape dash_attn_bwd rejects.
+ */
+int dash_select_schedule(int B, int Hq, int Hkv, int S, int D, int causal);
 
 /*
  * dash_attn_bwd_preprocess -- delta[b,h,s] = sum_d dO[b,h,s,d] * O[b,h,s,d].
@@ -87,7 +108,8 @@ int dash_attn_bwd_preprocess(const dash_bf16* o, const dash_bf16* dO, float* del
  *   dk, dv bf16 [B,Hkv,S,D] -- accumulated on chip per KV tile over the
  *       tile's pairs in the schedule's visit order and over the query heads
  *       of its group in ascending head order; rounded to nearest even.
- * schedule: a dash_schedule value.  causal: 0 (full) or 1 (top-left causal).
+ * schedule: a dash_schedule value (DASH_SCHED_AUTO runs the schedule
+ * dash_select_schedule returns).  causal: 0 (full) or 1 (top-left causal).
  *
  * For every schedule except DASH_SCHED_ATOMIC_NONDET the three outputs are
  * bitwise identical across runs on the same device model and SM count,

@@ -79,6 +79,17 @@ def test_symmetric_shift_is_shift_on_full_masks():
             assert same_bits(x, y)
 
 
+def test_auto_runs_the_selected_schedule():
+    for name in ("full_s512_d64", "causal_s640_d64_gqa", "causal_s384_d128_gqa", "causal_s1024_d128"):
+        c = case(name)
+        chosen = dash.select_schedule(c.B, c.Hq, c.Hkv, c.S, c.D, c.causal)
+        a = run(c, "auto")
+        b = run(c, chosen)
+        for x, y in zip(a, b):
+            assert same_bits(x, y), (name, chosen)
+        check(name + " auto dq", a[1], c.ref[0])
+
+
 @pytest.mark.parametrize("name", list(SHAPES))
 @pytest.mark.parametrize("sched", ORDERED)
 def test_order_log_matches_simulator(name, sched):

@@ -121,7 +121,7 @@ int validate_shape(int B, int Hq, int Hkv, int S, int D, int causal, int schedul
     if (D != 64 && D != 128) return DASH_ERR_ARG;
     if (Hq % Hkv != 0) return DASH_ERR_ARG;
     if (causal != 0 && causal != 1) return DASH_ERR_ARG;
-    if (schedule < 0 || schedule > 4) return DASH_ERR_ARG;
+    if (schedule < 0 || schedule > kAuto) return DASH_ERR_ARG;
     if ((long long)B * Hq * S >= (1ll << 31)) return DASH_ERR_ARG;
     if (S / 128 > 65535) return DASH_ERR_ARG;
     return DASH_OK;
@@ -135,6 +135,7 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
         if (!aligned16(ptr)) return DASH_ERR_ARG;
     int rc = validate_shape(B, Hq, Hkv, S, D, causal, schedule);
     if (rc) return rc;
+    if (schedule == kAuto) schedule = select_schedule(D, causal);
     int dev = 0;
     if ((rc = check_device(&dev))) return rc;
     int P = 0;
@@ -292,6 +293,11 @@ int dash_attn_bwd_debug(const dash_bf16* q, const dash_bf16* k, const dash_bf16*
                         const dash_debug_opts* opts) {
     return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, S, D, causal, schedule, (cudaStream_t)stream,
                     opts);
+}
+
+int dash_select_schedule(int B, int Hq, int Hkv, int S, int D, int causal) {
+    const int rc = validate_shape(B, Hq, Hkv, S, D, causal, kAuto);
+    return rc ? rc : select_schedule(D, causal);
 }
 
 int dash_dq_finalize(const float* dq_accum, dash_bf16* dq, size_t numel, dash_stream_t stream) {

@@ -71,8 +71,9 @@ extern "C" int dash_attn_bwd_noalloc(const dash_bf16* q, const dash_bf16* k, con
     for (const void* ptr : ptrs)
         if (!ptr || ((uintptr_t)ptr & 15u)) return DASH_ERR_ARG;
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 || S % 128 || (D != 64 && D != 128) || Hq % Hkv ||
-        (causal != 0 && causal != 1) || schedule < 0 || schedule > 4 || (long long)B * Hq * S >= (1ll << 31))
+        (causal != 0 && causal != 1) || schedule < 0 || schedule > kAuto || (long long)B * Hq * S >= (1ll << 31))
         return DASH_ERR_ARG;
+    if (schedule == kAuto) schedule = select_schedule(D, causal);
     int dev = 0, major = 0, minor = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||

@@ -36,7 +36,18 @@ enum Sched : int {
     kDescending = 2,
     kShift = 3,
     kSymmetric = 4,
+    kAuto = 5,   // resolved on the host by select_schedule before anything runs
 };
+
+// The deterministic schedule run for kAuto: a function of the shape only, so
+// that kAuto is as reproducible as the schedule it names.  Measured on GB300
+// (kernel-only): full masks run shift (symmetric shift is the same schedule);
+// causal masks run symmetric shift at D = 128 (ahead of shift by 9%, of
+// descending by 2x) and shift at D = 64 (ahead of symmetric shift by 10%).
+inline int select_schedule(int D, int causal) {
+    if (!causal) return kShift;
+    return D == 128 ? kSymmetric : kShift;
+}
 
 struct Shape {
     int B, Hq, Hkv, n, G, causal, sched;

@@ -25,7 +25,7 @@ _NAMES = {0: "DASH_OK", -1: "DASH_ERR_ARG", -2: "DASH_ERR_CUDA", -3: "DASH_ERR_L
 EXPORTS = (
     "dash_attn_bwd_preprocess", "dash_attn_bwd", "dash_dq_finalize", "dash_get_status", "dash_set_timeout_ns",
     "dash_release_workspaces", "dash_num_ctas", "dash_sim_schedule", "dash_sim_check_ranks",
-    "dash_attn_bwd_debug", "dash_debug_tile_probe", "dash_attn_bwd_noalloc",
+    "dash_attn_bwd_debug", "dash_debug_tile_probe", "dash_attn_bwd_noalloc", "dash_select_schedule",
 )
 
 
@@ -169,6 +169,13 @@ def set_timeout_ns(ns):
 
 def release_workspaces():
     _check(lib().dash_release_workspaces(), "dash_release_workspaces")
+
+
+def select_schedule(B, Hq, Hkv, S, D, causal):
+    """Name of the deterministic schedule that schedule="auto" runs for this shape."""
+    rc = lib().dash_select_schedule(B, Hq, Hkv, S, D, int(bool(causal)))
+    _check(rc if rc < 0 else 0, "dash_select_schedule")
+    return {v: k for k, v in SCHEDULE_IDS.items()}[rc]
 
 
 def num_ctas(device=None):

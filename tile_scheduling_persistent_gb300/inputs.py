@@ -21,6 +21,7 @@ SCHEDULE_IDS = {
     "descending_q": 2,
     "shift": 3,
     "symmetric_shift": 4,
+    "auto": 5,
 }
 
 
