@@ -51,6 +51,8 @@ def parse():
                     help="one step of --schedule with the kernel's per-role wait-cycle counters; prints a JSON line")
     ap.add_argument("--trace-out", default=None,
                     help="with --wait-profile: also write the event trace of CTA 0 (JSON) to this path")
+    ap.add_argument("--forward-only", action="store_true",
+                    help="time only dash_attn_fwd on the workload and print one JSON line (profiling aid)")
     ap.add_argument("--kernel-only", action="store_true",
                     help="only W + K steps of --schedule (for profiler captures); prints a short JSON line")
     return ap.parse_args()
@@ -133,30 +135,41 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- GPU arm
 def gpu_inputs(w, seed, device):
-    """Seeded bf16 inputs; O and LSE from a plain fp32 PyTorch forward on the GPU
-    (input synthesis only, outside every timed region)."""
+    """Seeded bf16 inputs; O and LSE from this library's forward pass on the GPU
+    (input synthesis, outside every timed region)."""
     import torch
+    from tile_scheduling_persistent_gb300 import dash
     from tile_scheduling_persistent_gb300.inputs import make_qkvdo
     q, k, v, do = (t.to(device) for t in make_qkvdo(w.B, w.Hq, w.Hkv, w.S, w.D, seed, w.sigma_qkv, w.sigma_do))
-    G = w.Hq // w.Hkv
     o = torch.empty_like(q)
     lse = torch.empty(w.B, w.Hq, w.S, dtype=torch.float32, device=device)
-    scale = 1.0 / math.sqrt(w.D)
-    rows = 2048
-    ar = torch.arange(w.S, device=device)
-    for b in range(w.B):
-        for h in range(w.Hq):
-            K = k[b, h // G].float()
-            V = v[b, h // G].float()
-            for r0 in range(0, w.S, rows):
-                s = (q[b, h, r0:r0 + rows].float() @ K.T) * scale
-                if w.causal:
-                    s.masked_fill_(ar[None, :] > ar[r0:r0 + rows, None], float("-inf"))
-                lse_blk = torch.logsumexp(s, dim=-1)
-                lse[b, h, r0:r0 + rows] = lse_blk
-                o[b, h, r0:r0 + rows] = (torch.exp(s - lse_blk[:, None]) @ V).to(torch.bfloat16)
-    torch.cuda.synchronize()
+    dash.attn_fwd(q, k, v, o, lse, w.causal)
+    code, info = dash.get_status()
+    if code != 0:
+        raise RuntimeError("forward: device status %d %s" % (code, info))
     return q, k, v, o, do, lse
+
+
+def time_forward(w, tensors, steps, warmup, stream):
+    """ms per forward call (dash_attn_fwd: O and LSE), CUDA events on `stream`."""
+    import torch
+    from tile_scheduling_persistent_gb300 import dash
+    q, k, v, _, _, _ = tensors
+    o = torch.empty_like(q)
+    lse = torch.empty(w.B, w.Hq, w.S, dtype=torch.float32, device=q.device)
+    for _ in range(warmup):
+        dash.attn_fwd(q, k, v, o, lse, w.causal, stream=stream)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        dash.attn_fwd(q, k, v, o, lse, w.causal, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    code, info = dash.get_status(stream)
+    if code != 0:
+        raise RuntimeError("forward: device status %d %s" % (code, info))
+    return a.elapsed_time(b) / steps
 
 
 def time_schedule(w, sched, tensors, outs, steps, warmup, stream, kernel_events=False):
@@ -230,6 +243,11 @@ def main_gpu(args):
         print(json.dumps(wait_profile(w, args.schedule or det[0], tensors, outs, args.warmup, stream,
                                       args.trace_out)))
         return
+    if args.forward_only:
+        ms = time_forward(w, tensors, args.steps, args.warmup, stream)
+        print(json.dumps({"workload": w.name, "forward_ms": round(ms, 4),
+                          "tflops": round(0.4 * flop / (ms * 1e-3) / 1e12, 2)}))
+        return
     if args.kernel_only:
         sched = args.schedule or det[0]
         ms, _, lps = time_schedule(w, sched, tensors, outs, args.steps, args.warmup, stream)
@@ -272,6 +290,7 @@ def main_gpu(args):
 
     # end to end through the public API: host inputs in, gradients out, every step
     e2e = e2e_run(w, best, tensors, args.steps, args.warmup, stream)
+    fwd_ms = max_over_ranks(time_forward(w, tensors, args.steps, args.warmup, stream))
     e2e_ms = max_over_ranks(e2e["ms"])
 
     burst, sustained, src = peaks()
@@ -307,6 +326,9 @@ def main_gpu(args):
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e_ms, 4),
                 "overlap": "double-buffered: copy-in of step k+1 and copy-out of step k-1 overlap step k"},
         "gpu_launches": lps * args.steps,
+        # the forward pass that produces this step's O and LSE (not in `value`): 4*S^2*D per head, halved causal
+        "forward": {"tflops": round(world * 0.4 * flop / (fwd_ms * 1e-3) / 1e12, 2), "ms": round(fwd_ms, 4),
+                    "kernel": "dash_fwd_kernel", "deterministic": True},
     }
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)

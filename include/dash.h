@@ -64,6 +64,27 @@ typedef enum {
 } dash_schedule;
 
 /*
+ * dash_attn_fwd -- the attention forward pass whose backward dash_attn_bwd
+ * computes (the textbook softmax attention that the gist.science DASH
+ * summary, section 1, takes as given; the pages schedule only the backward):
+ *   o[b,h,i,:]  = sum_j P[i,j] v[b,hk,j,:],  P = softmax_j(scale <q_i, k_j>),
+ *   lse[b,h,i]  = log sum_j exp(scale <q_i, k_j>)   (natural log),
+ * with scale = 1/sqrt(D), hk = h / (Hq/Hkv), and the sum over j <= i when
+ * causal (top-left aligned).  Outputs are exactly the o and lse arguments
+ * that dash_attn_bwd expects.
+ *   q: device bf16 [B,Hq,S,D]; k, v: device bf16 [B,Hkv,S,D] (caller-owned,
+ *   contiguous, 16-byte aligned).  o: device bf16 [B,Hq,S,D] (written,
+ *   rounded to nearest even); lse: device fp32 [B,Hq,S] (written).
+ * One CTA per 128-row query tile; no cross-CTA reduction, so the outputs are
+ * bitwise reproducible.  Same shape rules as dash_attn_bwd (S % 128 == 0,
+ * D in {64, 128}, Hq % Hkv == 0).  Asynchronous on `stream`; returns
+ * DASH_OK, DASH_ERR_ARG, DASH_ERR_DEVICE, DASH_ERR_NOMEM or DASH_ERR_CUDA;
+ * a device-side timeout is reported by dash_get_status on the same stream.
+ */
+int dash_attn_fwd(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, dash_bf16* o, float* lse,
+                  int B, int Hq, int Hkv, int S, int D, int causal, dash_stream_t stream);
+
+/*
  * dash_select_schedule -- the deterministic schedule that DASH_SCHED_AUTO
  * runs for this shape.  The DASH pages make the choice of strategy a matter
  * of the hardware: on H800 symmetric shift falls behind descending Q-tile

@@ -20,7 +20,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT = os.path.join(PKG, "libdash.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
-CUDA_SOURCES = ["dash_bwd.cu", "dash_aux.cu", "dash_probe.cu", "dash_api.cu", "dash_noalloc.cu"]
+CUDA_SOURCES = ["dash_bwd.cu", "dash_fwd.cu", "dash_aux.cu", "dash_probe.cu", "dash_api.cu", "dash_noalloc.cu"]
 CXX_SOURCES = ["dash_sim.cpp"]
 
 

@@ -295,6 +295,24 @@ int dash_attn_bwd_debug(const dash_bf16* q, const dash_bf16* k, const dash_bf16*
                     opts);
 }
 
+int dash_attn_fwd(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, dash_bf16* o, float* lse, int B,
+                  int Hq, int Hkv, int S, int D, int causal, dash_stream_t stream_) {
+    cudaStream_t stream = (cudaStream_t)stream_;
+    const void* ptrs[] = {q, k, v, o, lse};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return DASH_ERR_ARG;
+    int rc = validate_shape(B, Hq, Hkv, S, D, causal, 0);
+    if (rc) return rc;
+    int dev = 0;
+    if ((rc = check_device(&dev))) return rc;
+    Workspace* ws = get_ws(dev, stream);
+    if (ws->ints.ensure((size_t)kIntHeader * sizeof(int))) return DASH_ERR_NOMEM;
+    if (cudaMemsetAsync(ws->ints.p, 0, 8 * sizeof(int), stream) != cudaSuccess) return DASH_ERR_CUDA;
+    rc = launch_fwd(q, k, v, o, lse, (int*)ws->ints.p, B, Hq, Hkv, S, D, causal, g_timeout_ns.load(), stream);
+    if (rc == -1) return DASH_ERR_ARG;
+    return rc ? DASH_ERR_CUDA : DASH_OK;
+}
+
 int dash_select_schedule(int B, int Hq, int Hkv, int S, int D, int causal) {
     const int rc = validate_shape(B, Hq, Hkv, S, D, causal, kAuto);
     return rc ? rc : select_schedule(D, causal);

@@ -1,0 +1,408 @@
+// dash_fwd.cu -- the attention forward pass (O and the log-sum-exp LSE) on
+// sm_103a, producing exactly the inputs the deterministic backward consumes,
+// so that a training step runs on one GPU without another library.
+//
+// One CTA per 128-row Q tile (head-major over the grid, so that resident
+// CTAs share K/V in L2; within a head, causal tiles longest first).  For KV tiles j = 0 .. (causal ? i : n-1):
+//
+//   S = Q K_j^T                 (tcgen05, both operands K-major, two TMEM buffers)
+//   m = running row max of scale*log2e*S, l = running row sum of
+//   P = exp2(scale*log2e*S - m) (zero right of the diagonal on the diagonal tile)
+//   O += P V_j                  (A = P packed bf16 in tensor memory, B = V MN-major)
+//
+// The row max is only raised (and O, l rescaled) when a row's new maximum
+// exceeds the reference by more than 8 (a factor 2^8), which keeps P <= 256
+// and makes rescaling rare; the final O / l and LSE = ln2 * (m + log2 l) do
+// not depend on when it happens.  No CTA reads another's results, so the
+// outputs are bitwise reproducible.  This is the textbook softmax attention
+// that the gist.science DASH summary (section 1) takes as the forward pass
+// whose backward it schedules.
+//
+// Warps: 0 producer (TMA: Q once, K/V double-buffered), 1 MMA issuer and
+// TMEM owner, 2-3 idle, 4-7 softmax and epilogue (one Q row per thread,
+// TMEM lanes 32*(w%4) ..).  Tensor memory: O [0, D), S/P buffers at columns
+// 256 and 384.  Every wait is bounded (%globaltimer); on expiry the status
+// word records DASH_ERR_TIMEOUT and the CTA drains and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "dash_bwd.cuh"
+#include "dash_internal.h"
+
+namespace dash {
+
+namespace {
+
+struct FwdParams {
+    CUtensorMap tm_q, tm_k, tm_v;   // 2D [rows, D] bf16, box 64 x 128, SWIZZLE_128B
+    __nv_bfloat16* o;
+    float* lse;
+    int* status;                    // [8]: code, info[4]
+    unsigned long long timeout_ns;
+    int B, Hq, Hkv, S, n, G, causal;
+    float scale_log2e;
+};
+
+enum FwdBar : int {
+    F_Q_FULL = 0,
+    F_K_FULL = 1,      // 2 stages
+    F_V_FULL = 3,      // 2 stages
+    F_KV_EMPTY = 5,    // 2 stages
+    F_S_FULL = 7,      // 2 buffers
+    F_P_READY = 9,     // 2 buffers
+    F_O_DONE = 11,
+    F_DRAIN = 12,
+    F_COUNT = 13
+};
+
+template <int D>
+struct FwdCfg {
+    static constexpr int kTile = D * 128 * 2;
+    static constexpr int kNBox = D / 64;
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = kTile;                 // 2 stages
+    static constexpr int OFF_V = OFF_K + 2 * kTile;     // 2 stages
+    static constexpr int OFF_CTL = OFF_V + 2 * kTile;
+    // at least ~117 KB so that one CTA (and its 512 TMEM columns) holds an SM
+    static constexpr int kSmem = (OFF_CTL + 256 > 120000) ? OFF_CTL + 256 : 120000;
+    static constexpr uint32_t COL_O = 0;
+    static constexpr uint32_t COL_S = 256;              // buffers at 256 and 384
+    static_assert(D <= 256, "tensor memory budget");
+};
+
+constexpr int kCtlTmemF = 128, kCtlAbortF = 132;
+constexpr float kLn2 = 0.69314718055994531f;
+
+struct FwdWait {
+    volatile int* abort_smem;
+    int* status;
+    unsigned long long timeout;
+};
+
+__device__ __noinline__ void fwd_timeout(const FwdWait& w, int role, int i0) {
+    if (atomicCAS(w.status, 0, -4) == 0) {   // DASH_ERR_TIMEOUT, first failure wins
+        w.status[1] = i0;
+        w.status[2] = (int)blockIdx.x;
+        w.status[3] = -1;
+        w.status[4] = role;
+        __threadfence();
+    }
+    *w.abort_smem = 1;
+}
+
+__device__ bool fwait1(uint32_t bar, uint32_t parity, const FwdWait& w, int role, int i0) {
+    if (ptx::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = ptx::globaltimer();
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        if (*w.abort_smem) return false;
+        if (ptx::globaltimer() - t0 > w.timeout) {
+            fwd_timeout(w, role, i0);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Whole warp: lane 0 polls, then every lane observes the phase (acquire).
+__device__ bool fwaitw(uint32_t bar, uint32_t parity, const FwdWait& w, int role, int i0) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) ok = fwait1(bar, parity, w, role, i0) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (ok)
+        while (!ptx::mbar_try_wait(bar, parity)) {
+        }
+    return ok != 0;
+}
+
+template <int D>
+__global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant__ FwdParams p) {
+    using C = FwdCfg<D>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    uint8_t* ctl = smem + C::OFF_CTL;
+    const uint32_t bar0 = ptx::smem_u32(ctl);
+    auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
+    volatile uint32_t* tmem_slot = reinterpret_cast<volatile uint32_t*>(ctl + kCtlTmemF);
+    volatile int* abort_smem = reinterpret_cast<volatile int*>(ctl + kCtlAbortF);
+    const FwdWait fw{abort_smem, p.status, p.timeout_ns};
+    const uint32_t sbase = ptx::smem_u32(smem);
+
+    // work item: head-major, so that the CTAs resident together share their
+    // heads' K/V in L2 (query heads of one group are adjacent); within a head
+    // the Q tiles run in descending order (longest causal rows first)
+    const int qt = p.n - 1 - (int)(blockIdx.x % p.n);
+    const int bh = (int)(blockIdx.x / p.n);
+    const int b = bh / p.Hq, hq = bh % p.Hq, hkv = hq / p.G;
+    const int nkv = p.causal ? qt + 1 : p.n;
+    const int qrow = (b * p.Hq + hq) * p.S + qt * 128;
+    const int kvrow0 = (b * p.Hkv + hkv) * p.S;
+
+    if (threadIdx.x == 0) {
+        *abort_smem = (sbase & 1023u) ? 1 : 0;
+        if (sbase & 1023u) fwd_timeout(fw, -1, (int)sbase);
+        ptx::mbar_init(BAR(F_Q_FULL), 1);
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(BAR(F_K_FULL + s), 1);
+            ptx::mbar_init(BAR(F_V_FULL + s), 1);
+            ptx::mbar_init(BAR(F_KV_EMPTY + s), 1);
+            ptx::mbar_init(BAR(F_S_FULL + s), 1);
+            ptx::mbar_init(BAR(F_P_READY + s), 4);
+        }
+        ptx::mbar_init(BAR(F_O_DONE), 1);
+        ptx::mbar_init(BAR(F_DRAIN), 1);
+        ptx::fence_mbar_init();
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_u32((const void*)tmem_slot), 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        // ================================================== producer
+        if (lane == 0 && !*abort_smem) {
+            ptx::prefetch_tensormap(&p.tm_q);
+            ptx::prefetch_tensormap(&p.tm_k);
+            ptx::prefetch_tensormap(&p.tm_v);
+            ptx::mbar_arrive_expect_tx(BAR(F_Q_FULL), C::kTile);
+#pragma unroll
+            for (int bx = 0; bx < C::kNBox; ++bx)
+                ptx::tma_load_2d(sbase + C::OFF_Q + bx * kBox, &p.tm_q, 64 * bx, qrow, BAR(F_Q_FULL));
+            int issued = 0;
+            for (int j = 0; j < nkv; ++j) {
+                const int st = j & 1;
+                if (j >= 2 && !fwait1(BAR(F_KV_EMPTY + st), (uint32_t)((j / 2 - 1) & 1), fw, 1, j)) break;
+                const int row = kvrow0 + j * 128;
+                ptx::mbar_arrive_expect_tx(BAR(F_K_FULL + st), C::kTile);
+#pragma unroll
+                for (int bx = 0; bx < C::kNBox; ++bx)
+                    ptx::tma_load_2d(sbase + C::OFF_K + st * C::kTile + bx * kBox, &p.tm_k, 64 * bx, row,
+                                     BAR(F_K_FULL + st));
+                ptx::mbar_arrive_expect_tx(BAR(F_V_FULL + st), C::kTile);
+#pragma unroll
+                for (int bx = 0; bx < C::kNBox; ++bx)
+                    ptx::tma_load_2d(sbase + C::OFF_V + st * C::kTile + bx * kBox, &p.tm_v, 64 * bx, row,
+                                     BAR(F_V_FULL + st));
+                issued = j + 1;
+            }
+            // let every issued load land before the CTA can exit (bounded)
+            const uint64_t t0 = ptx::globaltimer();
+            auto drain = [&](uint32_t bar, uint32_t parity) {
+                while (!ptx::mbar_try_wait(bar, parity) && ptx::globaltimer() - t0 < 100000000ull) {
+                }
+            };
+            drain(BAR(F_Q_FULL), 0);
+            for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j) {
+                drain(BAR(F_K_FULL + (j & 1)), (uint32_t)((j / 2) & 1));
+                drain(BAR(F_V_FULL + (j & 1)), (uint32_t)((j / 2) & 1));
+            }
+        }
+    } else if (warp == 1) {
+        // ================================================== MMA issuer
+        if (lane == 0 && !*abort_smem) {
+            const uint32_t sQ = sbase + C::OFF_Q;
+            auto tS = [&](int j) { return tmem + C::COL_S + 128u * (uint32_t)(j & 1); };
+            auto sK = [&](int j) { return sbase + C::OFF_K + (uint32_t)(j & 1) * C::kTile; };
+            auto sV = [&](int j) { return sbase + C::OFF_V + (uint32_t)(j & 1) * C::kTile; };
+            bool ok = fwait1(BAR(F_Q_FULL), 0, fw, 2, 0) && fwait1(BAR(F_K_FULL), 0, fw, 2, 0);
+            if (ok) {
+                ptx::tc_fence_after();
+                issue_s<D>(tS(0), sQ, sK(0));
+                ptx::tc_commit(BAR(F_S_FULL));
+            }
+            for (int j = 0; ok && j < nkv; ++j) {
+                if (j + 1 < nkv) {
+                    // S(j+1) overwrites the buffer PV(j-1) read; MMAs run in issue order
+                    if (!fwait1(BAR(F_K_FULL + ((j + 1) & 1)), (uint32_t)(((j + 1) / 2) & 1), fw, 2, j)) break;
+                    ptx::tc_fence_after();
+                    issue_s<D>(tS(j + 1), sQ, sK(j + 1));
+                    ptx::tc_commit(BAR(F_S_FULL + ((j + 1) & 1)));
+                }
+                if (!fwait1(BAR(F_P_READY + (j & 1)), (uint32_t)((j / 2) & 1), fw, 2, j)) break;
+                if (!fwait1(BAR(F_V_FULL + (j & 1)), (uint32_t)((j / 2) & 1), fw, 2, j)) break;
+                ptx::tc_fence_after();
+                issue_dv<D>(tmem + C::COL_O, tS(j), sV(j), j > 0 ? 1u : 0u);   // O (+)= P V_j
+                ptx::tc_commit(BAR(F_KV_EMPTY + (j & 1)));
+                ptx::tc_commit(BAR(F_O_DONE));
+            }
+            // wait for every issued MMA before tensor memory can be freed
+            ptx::tc_commit(BAR(F_DRAIN));
+            const uint64_t t0 = ptx::globaltimer();
+            while (!ptx::mbar_try_wait(BAR(F_DRAIN), 0) && ptx::globaltimer() - t0 < 100000000ull) {
+            }
+        }
+    } else if (warp >= 4) {
+        // ================================================== softmax + epilogue (one Q row per thread)
+        const int sub = warp & 3;
+        const int row = 32 * sub + lane;
+        const uint32_t lane_off = (uint32_t)(32 * sub) << 16;
+        const float c = p.scale_log2e;
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < nkv; ++j) {
+            const int buf = j & 1;
+            if (!fwaitw(BAR(F_S_FULL + buf), (uint32_t)((j / 2) & 1), fw, 3, j)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t ts = tmem + lane_off + C::COL_S + 128u * (uint32_t)buf;
+            float x[128];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                uint32_t r[32];
+                ptx::tmem_ld32(ts + 32 * h, r);
+                ptx::tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 32; ++k) x[32 * h + k] = __uint_as_float(r[k]);   // raw scores
+            }
+            if (p.causal && j == qt) {   // diagonal tile: key k visible to query row iff k <= row
+#pragma unroll
+                for (int k = 0; k < 128; ++k)
+                    if (k > row) x[k] = -INFINITY;
+            }
+            // row max and (below) row sum over 8 interleaved partials: short
+            // dependency chains, and a fixed order of the additions
+            float part[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) part[i] = x[i];
+#pragma unroll
+            for (int k = 8; k < 128; ++k) part[k & 7] = fmaxf(part[k & 7], x[k]);
+            const float mx = c * fmaxf(fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3])),
+                                       fmaxf(fmaxf(part[4], part[5]), fmaxf(part[6], part[7])));
+            // raise the reference maximum only when some row of the warp grew by > 2^8
+            const bool raise = __any_sync(0xffffffffu, mx > m_ref + 8.f);
+            float alpha = 1.f;
+            if (raise) {
+                const float m_new = fmaxf(m_ref, mx);
+                alpha = ptx::ex2(m_ref - m_new);   // 0 on the first tile (m_ref = -inf)
+                m_ref = m_new;
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) part[i] = 0.f;
+#pragma unroll
+            for (int k = 0; k < 128; ++k) {
+                x[k] = ptx::ex2(fmaf(x[k], c, -m_ref));
+                part[k & 7] += x[k];
+            }
+            const float rs = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
+            l = l * alpha + rs;
+            if (raise && j > 0) {
+                // O holds the sum through PV(j-1): wait for it, then rescale in place
+                // (S(j) was committed after PV(j-2), so phase j-1 is the next one)
+                if (!fwaitw(BAR(F_O_DONE), (uint32_t)((j - 1) & 1), fw, 3, j)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t r[32];
+                    ptx::tmem_ld32(tmem + lane_off + C::COL_O + 32 * cc, r);
+                    ptx::tmem_ld_wait();
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
+                    ptx::tmem_st32(tmem + lane_off + C::COL_O + 32 * cc, r);
+                }
+            }
+            // packed bf16 P: keys [0,64) -> columns [0,32), keys [64,128) -> [64,96)
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    __nv_bfloat162 h2 = __floats2bfloat162_rn(x[32 * q4 + 2 * k], x[32 * q4 + 2 * k + 1]);
+                    pk[k] = *reinterpret_cast<uint32_t*>(&h2);
+                }
+                ptx::tmem_st16(ts + 64 * (q4 >> 1) + 16 * (q4 & 1), pk);
+            }
+            ptx::tmem_st_wait();
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(BAR(F_P_READY + buf));
+        }
+        // The last S this thread saw was committed after PV(nkv-3): step through
+        // the phases of PV(nkv-2) and PV(nkv-1) so that parity cannot alias.
+        for (int jj = (nkv > 2 ? nkv - 2 : 0); ok && jj < nkv; ++jj)
+            ok = fwaitw(BAR(F_O_DONE), (uint32_t)(jj & 1), fw, 3, nkv);
+        if (ok) {
+            ptx::tc_fence_after();
+            const float inv = 1.f / l;
+            __nv_bfloat16* orow = p.o + ((size_t)qrow + row) * D;
+#pragma unroll
+            for (int cc = 0; cc < D / 32; ++cc) {
+                uint32_t r[32];
+                ptx::tmem_ld32(tmem + lane_off + C::COL_O + 32 * cc, r);
+                ptx::tmem_ld_wait();
+                uint32_t pk[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    __nv_bfloat162 h2 =
+                        __floats2bfloat162_rn(__uint_as_float(r[2 * k]) * inv, __uint_as_float(r[2 * k + 1]) * inv);
+                    pk[k] = *reinterpret_cast<uint32_t*>(&h2);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    *reinterpret_cast<uint4*>(orow + 32 * cc + 8 * e) =
+                        make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+            }
+            p.lse[qrow + row] = (m_ref + log2f(l)) * kLn2;
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D>
+int launch_fwd_t(const FwdParams& prm, int grid, cudaStream_t stream) {
+    static bool attr_done[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -2;
+    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
+        if (cudaFuncSetAttribute(dash_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 FwdCfg<D>::kSmem) != cudaSuccess)
+            return -2;
+        attr_done[dev] = true;
+    }
+    dash_fwd_kernel<D><<<grid, 256, FwdCfg<D>::kSmem, stream>>>(prm);
+    return cudaGetLastError() == cudaSuccess ? 0 : -2;
+}
+
+}  // namespace
+
+int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int* status, int B, int Hq,
+               int Hkv, int S, int D, int causal, unsigned long long timeout_ns, cudaStream_t stream) {
+    FwdParams prm;
+    if (make_tmap_2d(&prm.tm_q, q, (long long)B * Hq * S, D) || make_tmap_2d(&prm.tm_k, k, (long long)B * Hkv * S, D) ||
+        make_tmap_2d(&prm.tm_v, v, (long long)B * Hkv * S, D))
+        return -2;
+    prm.o = (__nv_bfloat16*)o;
+    prm.lse = lse;
+    prm.status = status;
+    prm.timeout_ns = timeout_ns;
+    prm.B = B;
+    prm.Hq = Hq;
+    prm.Hkv = Hkv;
+    prm.S = S;
+    prm.n = S / 128;
+    prm.G = Hq / Hkv;
+    prm.causal = causal;
+    prm.scale_log2e = (1.0f / sqrtf((float)D)) * kLog2e;
+    const long long grid = (long long)B * Hq * (S / 128);
+    if (grid <= 0 || grid > 0x7fffffffll) return -1;
+    return D == 64 ? launch_fwd_t<64>(prm, (int)grid, stream) : launch_fwd_t<128>(prm, (int)grid, stream);
+}
+
+}  // namespace dash

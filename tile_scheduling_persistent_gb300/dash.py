@@ -26,6 +26,7 @@ EXPORTS = (
     "dash_attn_bwd_preprocess", "dash_attn_bwd", "dash_dq_finalize", "dash_get_status", "dash_set_timeout_ns",
     "dash_release_workspaces", "dash_num_ctas", "dash_sim_schedule", "dash_sim_check_ranks",
     "dash_attn_bwd_debug", "dash_debug_tile_probe", "dash_attn_bwd_noalloc", "dash_select_schedule",
+    "dash_attn_fwd",
 )
 
 
@@ -169,6 +170,15 @@ def set_timeout_ns(ns):
 
 def release_workspaces():
     _check(lib().dash_release_workspaces(), "dash_release_workspaces")
+
+
+def attn_fwd(q, k, v, o, lse, causal, stream=None):
+    """o (bf16 [B,Hq,S,D]) and lse (fp32 [B,Hq,S], natural log) <- forward."""
+    B, Hq, S, D = q.shape
+    Hkv = k.shape[1]
+    bf = torch.bfloat16
+    _check(lib().dash_attn_fwd(_ptr(q, bf), _ptr(k, bf), _ptr(v, bf), _ptr(o, bf), _ptr(lse, torch.float32),
+                               B, Hq, Hkv, S, D, int(bool(causal)), _stream(stream)), "dash_attn_fwd")
 
 
 def select_schedule(B, Hq, Hkv, S, D, causal):
