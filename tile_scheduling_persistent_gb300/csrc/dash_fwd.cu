@@ -18,9 +18,10 @@
 // that the gist.science DASH summary (section 1) takes as the forward pass
 // whose backward it schedules.
 //
-// Warps: 0 producer (TMA: Q once, K/V double-buffered), 1 MMA issuer and
-// TMEM owner, 2-3 idle, 4-7 softmax and epilogue (one Q row per thread,
-// TMEM lanes 32*(w%4) ..).  Tensor memory: O [0, D), S/P buffers at columns
+// Warps: 0 producer (TMA: Q once, K and V double-buffered; a K stage is
+// released as soon as its S product completes, a V stage after its PV), 1 MMA
+// issuer and TMEM owner, 2-3 idle, 4-7 softmax and epilogue (one Q row per
+// thread, TMEM lanes 32*(w%4) ..).  Tensor memory: O [0, D), S/P buffers at columns
 // 256 and 384.  Every wait is bounded (%globaltimer); on expiry the status
 // word records DASH_ERR_TIMEOUT and the CTA drains and exits.
 #include <cuda.h>
@@ -50,12 +51,13 @@ enum FwdBar : int {
     F_Q_FULL = 0,
     F_K_FULL = 1,      // 2 stages
     F_V_FULL = 3,      // 2 stages
-    F_KV_EMPTY = 5,    // 2 stages
+    F_K_EMPTY = 5,     // 2 stages: K stage free once S(j) is done
     F_S_FULL = 7,      // 2 buffers
     F_P_READY = 9,     // 2 buffers
     F_O_DONE = 11,
     F_DRAIN = 12,
-    F_COUNT = 13
+    F_V_EMPTY = 13,     // 2 stages: V stage free once PV(j) is done
+    F_COUNT = 15
 };
 
 template <int D>
@@ -148,7 +150,8 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
         for (int s = 0; s < 2; ++s) {
             ptx::mbar_init(BAR(F_K_FULL + s), 1);
             ptx::mbar_init(BAR(F_V_FULL + s), 1);
-            ptx::mbar_init(BAR(F_KV_EMPTY + s), 1);
+            ptx::mbar_init(BAR(F_K_EMPTY + s), 1);
+            ptx::mbar_init(BAR(F_V_EMPTY + s), 1);
             ptx::mbar_init(BAR(F_S_FULL + s), 1);
             ptx::mbar_init(BAR(F_P_READY + s), 4);
         }
@@ -178,13 +181,14 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
             int issued = 0;
             for (int j = 0; j < nkv; ++j) {
                 const int st = j & 1;
-                if (j >= 2 && !fwait1(BAR(F_KV_EMPTY + st), (uint32_t)((j / 2 - 1) & 1), fw, 1, j)) break;
+                if (j >= 2 && !fwait1(BAR(F_K_EMPTY + st), (uint32_t)((j / 2 - 1) & 1), fw, 1, j)) break;
                 const int row = kvrow0 + j * 128;
                 ptx::mbar_arrive_expect_tx(BAR(F_K_FULL + st), C::kTile);
 #pragma unroll
                 for (int bx = 0; bx < C::kNBox; ++bx)
                     ptx::tma_load_2d(sbase + C::OFF_K + st * C::kTile + bx * kBox, &p.tm_k, 64 * bx, row,
                                      BAR(F_K_FULL + st));
+                if (j >= 2 && !fwait1(BAR(F_V_EMPTY + st), (uint32_t)((j / 2 - 1) & 1), fw, 1, j)) break;
                 ptx::mbar_arrive_expect_tx(BAR(F_V_FULL + st), C::kTile);
 #pragma unroll
                 for (int bx = 0; bx < C::kNBox; ++bx)
@@ -216,6 +220,7 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
                 ptx::tc_fence_after();
                 issue_s<D>(tS(0), sQ, sK(0));
                 ptx::tc_commit(BAR(F_S_FULL));
+                ptx::tc_commit(BAR(F_K_EMPTY));
             }
             for (int j = 0; ok && j < nkv; ++j) {
                 if (j + 1 < nkv) {
@@ -224,12 +229,13 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
                     ptx::tc_fence_after();
                     issue_s<D>(tS(j + 1), sQ, sK(j + 1));
                     ptx::tc_commit(BAR(F_S_FULL + ((j + 1) & 1)));
+                    ptx::tc_commit(BAR(F_K_EMPTY + ((j + 1) & 1)));
                 }
                 if (!fwait1(BAR(F_P_READY + (j & 1)), (uint32_t)((j / 2) & 1), fw, 2, j)) break;
                 if (!fwait1(BAR(F_V_FULL + (j & 1)), (uint32_t)((j / 2) & 1), fw, 2, j)) break;
                 ptx::tc_fence_after();
                 issue_dv<D>(tmem + C::COL_O, tS(j), sV(j), j > 0 ? 1u : 0u);   // O (+)= P V_j
-                ptx::tc_commit(BAR(F_KV_EMPTY + (j & 1)));
+                ptx::tc_commit(BAR(F_V_EMPTY + (j & 1)));
                 ptx::tc_commit(BAR(F_O_DONE));
             }
             // wait for every issued MMA before tensor memory can be freed
