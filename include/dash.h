@@ -15,9 +15,11 @@
  *  - Tensor pointers are DEVICE pointers owned by the caller, contiguous
  *    row-major [B, H, S, D] (LSE and delta: [B, H, S]), 16-byte aligned.
  *  - dash_bf16 is the raw 16-bit storage of a bfloat16 value.
- *  - S must be a positive multiple of 128 (tiles are 128 x 128); D is 64 or
- *    128; Hq must be a multiple of Hkv (query heads hq = g*G .. g*G+G-1 share
- *    key/value head g, G = Hq / Hkv).
+ *  - S is any positive length; the kernels work on 128 x 128 tiles, n =
+ *    ceil(S / 128) per head, and mask the rows and columns of a partial last
+ *    tile (the schedules and accumulation orders are those of n tiles).  D
+ *    is 64 or 128; Hq must be a multiple of Hkv (query heads hq = g*G ..
+ *    g*G+G-1 share key/value head g, G = Hq / Hkv).
  *  - LSE is the natural-log log-sum-exp of scale * Q K^T per query row with
  *    scale = 1/sqrt(D) (the forward's statistic); masks are "full" or
  *    top-left causal (key j visible to query i iff j <= i).
@@ -76,7 +78,7 @@ typedef enum {
  *   contiguous, 16-byte aligned).  o: device bf16 [B,Hq,S,D] (written,
  *   rounded to nearest even); lse: device fp32 [B,Hq,S] (written).
  * One CTA per 128-row query tile; no cross-CTA reduction, so the outputs are
- * bitwise reproducible.  Same shape rules as dash_attn_bwd (S % 128 == 0,
+ * bitwise reproducible.  Same shape rules as dash_attn_bwd (any S > 0,
  * D in {64, 128}, Hq % Hkv == 0).  Asynchronous on `stream`; returns
  * DASH_OK, DASH_ERR_ARG, DASH_ERR_DEVICE, DASH_ERR_NOMEM or DASH_ERR_CUDA;
  * a device-side timeout is reported by dash_get_status on the same stream.
@@ -111,7 +113,7 @@ int dash_select_schedule(int B, int Hq, int Hkv, int S, int D, int causal);
  * o, dO: bf16 [B,Hq,S,D]; delta: fp32 [B,Hq,S] written by the call.  Each row
  * is summed in fp32 in one fixed order, so the result is bitwise
  * reproducible.  Returns DASH_ERR_ARG on null/misaligned pointers or bad
- * sizes (S need not be a multiple of 128 here), DASH_ERR_CUDA on launch
+ * sizes (any S > 0), DASH_ERR_CUDA on launch
  * failure.
  */
 int dash_attn_bwd_preprocess(const dash_bf16* o, const dash_bf16* dO, float* delta,
@@ -138,8 +140,8 @@ int dash_attn_bwd_preprocess(const dash_bf16* o, const dash_bf16* dO, float* del
  * argument), zeroes dq, builds or reuses the schedule tables, and launches
  * one persistent CTA per SM (cooperative launch).
  *
- * Errors: DASH_ERR_ARG (null or non-16-byte-aligned pointer, S % 128 != 0,
- * D not in {64,128}, Hq % Hkv != 0, non-positive sizes, unknown schedule or
+ * Errors: DASH_ERR_ARG (null or non-16-byte-aligned pointer, S <= 0,
+ * more than 65535 tiles per head, D not in {64,128}, Hq % Hkv != 0, non-positive sizes, unknown schedule or
  * causal flag), DASH_ERR_DEVICE, DASH_ERR_LAUNCH, DASH_ERR_NOMEM,
  * DASH_ERR_CUDA.  A device-side wait that exceeds the timeout does not hang:
  * the kernel stops, leaves dq/dk/dv undefined and records DASH_ERR_TIMEOUT,

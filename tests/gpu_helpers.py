@@ -34,7 +34,7 @@ class Case:
 
     @property
     def n(self):
-        return self.S // 128
+        return (self.S + 127) // 128   # the last tile may be partial
 
 
 def make_case(B, Hq, Hkv, S, D, causal, seed=0, sigma_qkv=1.0, sigma_do=1.0, with_ref=True):

@@ -41,8 +41,8 @@ def test_argument_validation_without_a_gpu(L):
     assert L.dash_attn_bwd(*([None] + args[1:]), 1, 2, 2, 512, 64, 0, 3, None) == dash.ERR_ARG
     # misaligned pointer
     assert L.dash_attn_bwd(*([bad] + args[1:]), 1, 2, 2, 512, 64, 0, 3, None) == dash.ERR_ARG
-    # S not a multiple of 128, D unsupported, Hq % Hkv, unknown schedule, causal flag
-    for (B, Hq, Hkv, S, D, causal, sched) in [(1, 2, 2, 500, 64, 0, 3), (1, 2, 2, 512, 96, 0, 3),
+    # empty sequence, D unsupported, Hq % Hkv, unknown schedule, causal flag
+    for (B, Hq, Hkv, S, D, causal, sched) in [(1, 2, 2, 0, 64, 0, 3), (1, 2, 2, 512, 96, 0, 3),
                                               (1, 3, 2, 512, 64, 0, 3), (1, 2, 2, 512, 64, 0, 7),
                                               (1, 2, 2, 512, 64, 2, 3), (0, 2, 2, 512, 64, 0, 3)]:
         assert L.dash_attn_bwd(*args, B, Hq, Hkv, S, D, causal, sched, None) == dash.ERR_ARG

@@ -27,6 +27,12 @@ SHAPES = {
     "full_s256_d128": (1, 2, 2, 256, 128, False),
     "causal_s1024_d128": (1, 3, 3, 1024, 128, True),   # n = 8
     "causal_s128_d64": (1, 1, 1, 128, 64, True),       # a single (diagonal) tile
+    # ragged lengths: the last tile is partial (S % 128 != 0)
+    "full_s200_d64": (1, 2, 2, 200, 64, False),        # n = 2, 72-row tail
+    "causal_s333_d128_gqa": (1, 4, 2, 333, 128, True),  # n = 3, 77-row tail, GQA 2:1
+    "causal_s700_d64_gqa": (2, 2, 1, 700, 64, True),   # n = 6, 60-row tail, B = 2
+    "full_s130_d128": (1, 1, 1, 130, 128, False),      # n = 2, 2-row tail
+    "causal_s100_d64": (1, 1, 1, 100, 64, True),       # one partial diagonal tile
 }
 
 _cases = {}
@@ -231,7 +237,7 @@ def test_invalid_arguments_on_device():
     s = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     base = [p(c.q), p(c.k), p(c.v), p(c.o), p(c.do), p(c.lse), p(dq), p(dk), p(dv)]
     assert L.dash_attn_bwd(*base, 1, 2, 2, 512, 64, 0, 9, s) == dash.ERR_ARG
-    assert L.dash_attn_bwd(*base, 1, 2, 2, 500, 64, 0, 3, s) == dash.ERR_ARG
+    assert L.dash_attn_bwd(*base, 1, 2, 2, 512, 80, 0, 3, s) == dash.ERR_ARG
     mis = list(base)
     mis[0] = ctypes.c_void_p(c.q.data_ptr() + 2)
     assert L.dash_attn_bwd(*mis, 1, 2, 2, 512, 64, 0, 3, s) == dash.ERR_ARG

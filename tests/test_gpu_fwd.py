@@ -22,6 +22,11 @@ SHAPES = {
     "causal_s1024_d128": (1, 3, 3, 1024, 128, True),
     "causal_s128_d64": (1, 1, 1, 128, 64, True),
     "full_s128_d128": (1, 1, 1, 128, 128, False),
+    # ragged lengths: the last tile is partial (S % 128 != 0)
+    "full_s200_d64": (1, 2, 2, 200, 64, False),
+    "causal_s333_d128_gqa": (1, 4, 2, 333, 128, True),
+    "full_s130_d128": (1, 1, 1, 130, 128, False),
+    "causal_s100_d64": (1, 1, 1, 100, 64, True),
 }
 LSE_ABS = 1e-4   # fp32 LSE of O(10): the kernel's fp32 score sums against the exact fp64 value
 
@@ -73,7 +78,8 @@ def test_forward_bitwise_reproducible():
 
 
 @pytest.mark.parametrize("name,sched", [("causal_s384_d128_gqa", "symmetric_shift"),
-                                        ("full_s512_d64", "shift"), ("causal_s640_d64_gqa", "auto")])
+                                        ("full_s512_d64", "shift"), ("causal_s640_d64_gqa", "auto"),
+                                        ("causal_s333_d128_gqa", "shift"), ("full_s200_d64", "descending_q")])
 def test_forward_then_backward_on_the_gpu(name, sched):
     """A whole training step's attention on the GPU (forward, then the
     deterministic backward on the forward's own O and LSE) against the exact
@@ -99,8 +105,8 @@ def test_forward_then_backward_on_the_gpu(name, sched):
 
 def test_forward_rejects_bad_shapes():
     dev = torch.device("cuda")
-    q = torch.zeros(1, 2, 200, 64, dtype=torch.bfloat16, device=dev)
+    q = torch.zeros(1, 2, 256, 96, dtype=torch.bfloat16, device=dev)   # D = 96 is not supported
     o = torch.empty_like(q)
-    lse = torch.empty(1, 2, 200, dtype=torch.float32, device=dev)
+    lse = torch.empty(1, 2, 256, dtype=torch.float32, device=dev)
     with pytest.raises(dash.DashError):
         dash.attn_fwd(q, q, q, o, lse, False)

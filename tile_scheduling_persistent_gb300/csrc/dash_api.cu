@@ -117,13 +117,12 @@ int check_device(int* dev_out) {
 
 int validate_shape(int B, int Hq, int Hkv, int S, int D, int causal, int schedule) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0) return DASH_ERR_ARG;
-    if (S % 128 != 0) return DASH_ERR_ARG;
     if (D != 64 && D != 128) return DASH_ERR_ARG;
     if (Hq % Hkv != 0) return DASH_ERR_ARG;
     if (causal != 0 && causal != 1) return DASH_ERR_ARG;
     if (schedule < 0 || schedule > kAuto) return DASH_ERR_ARG;
     if ((long long)B * Hq * S >= (1ll << 31)) return DASH_ERR_ARG;
-    if (S / 128 > 65535) return DASH_ERR_ARG;
+    if ((S + 127) / 128 > 65535) return DASH_ERR_ARG;
     return DASH_OK;
 }
 
@@ -143,7 +142,7 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
     if (rc == -3) return DASH_ERR_LAUNCH;
     if (rc) return DASH_ERR_CUDA;
 
-    const int n = S / 128;
+    const int n = (S + 127) / 128;   // the last tile may be partial
     const Shape sh{B, Hq, Hkv, n, Hq / Hkv, causal, schedule};
     const long long tiles = (long long)B * Hq * n;
     const long long entries = tiles * n;
@@ -183,14 +182,14 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
 
     int* ints = (int*)ws->ints.p;
     if (cudaMemsetAsync(ints, 0, (size_t)(kIntHeader + (kSubTiles + 1) * tiles) * sizeof(int), stream) != cudaSuccess ||
-        cudaMemsetAsync(dq, 0, (size_t)tiles * 128 * D * sizeof(float), stream) != cudaSuccess)
+        cudaMemsetAsync(dq, 0, (size_t)B * Hq * S * D * sizeof(float), stream) != cudaSuccess)
         return DASH_ERR_CUDA;
-    if (launch_preprocess(o, dO, (float*)ws->delta.p, tiles * 128, D, stream)) return DASH_ERR_CUDA;
+    if (launch_preprocess(o, dO, (float*)ws->delta.p, (long long)B * Hq * S, D, stream)) return DASH_ERR_CUDA;
 
     BwdParams prm;
     memset(&prm, 0, sizeof(prm));
-    if (make_tmap_2d(&prm.tm_q, q, (long long)B * Hq * S, D) || make_tmap_2d(&prm.tm_k, k, (long long)B * Hkv * S, D) ||
-        make_tmap_2d(&prm.tm_v, v, (long long)B * Hkv * S, D) || make_tmap_2d(&prm.tm_do, dO, (long long)B * Hq * S, D))
+    if (make_tmap_3d(&prm.tm_q, q, (long long)B * Hq, S, D) || make_tmap_3d(&prm.tm_k, k, (long long)B * Hkv, S, D) ||
+        make_tmap_3d(&prm.tm_v, v, (long long)B * Hkv, S, D) || make_tmap_3d(&prm.tm_do, dO, (long long)B * Hq, S, D))
         return DASH_ERR_CUDA;
     prm.lse = lse;
     prm.delta = (const float*)ws->delta.p;
@@ -253,6 +252,22 @@ int encode_2d(void* map_out, CUtensorMapDataType dt, int esize, const void* base
     return r == CUDA_SUCCESS ? 0 : -2;
 }
 }  // namespace
+
+// bf16 [heads][S][D], boxes of 64 columns x 128 rows x 1 head (128 B rows,
+// swizzled).  Rows past S inside a head read as zero, so a ragged last tile
+// never touches the next head.  Strides S*D*2 and D*2 are multiples of 16.
+int make_tmap_3d(void* map_out, const void* base, long long heads, int S, int D) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return -2;
+    const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)S, (cuuint64_t)heads};
+    const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)S * D * 2};
+    const cuuint32_t box[3] = {64, 128, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(reinterpret_cast<CUtensorMap*>(map_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+                    const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? 0 : -2;
+}
 
 // bf16 [rows, D], boxes of 64 columns x 128 rows (128 B rows, swizzled).
 int make_tmap_2d(void* map_out, const void* base, long long rows, int D) {

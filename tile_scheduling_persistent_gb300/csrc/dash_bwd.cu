@@ -105,7 +105,9 @@ __device__ bool wait_turn(const BwdParams& p, const Ctl& c, volatile int* abort_
 
 }  // namespace
 
-template <int D, bool kProf>
+// kTail: compiled for S % 128 != 0 (masks and guards of the partial last
+// tile); the instantiation for whole tiles carries none of that code.
+template <int D, bool kProf, bool kTail>
 __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_constant__ BwdParams p) {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -219,7 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                     d.q = v.q;
                     d.kv = v.kv;
                     d.flags = (first ? kKvFirst : 0) | (last ? kKvLast : 0) |
-                              ((p.causal && v.q == v.kv) ? kDiag : 0);
+                              ((p.causal && v.q == v.kv) ? kDiag : 0) |
+                              ((kTail && (v.q == p.n - 1 || v.kv == p.n - 1)) ? kPartial : 0);
                     d.rank = rank;
                     d.pad = 0;
                     descs[ds] = d;
@@ -233,15 +236,15 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                         }
                         const uint32_t fb = BAR(B_KV_FULL);
                         ptx::mbar_arrive_expect_tx(fb, C::kKvBytes);
-                        const int row = (v.b * p.Hkv + v.hkv) * p.S + v.kv * 128;
+                        const int hk = v.b * p.Hkv + v.hkv;
 #pragma unroll
                         for (int bx = 0; bx < C::kNBox; ++bx) {
-                            ptx::tma_load_2d(sbase + C::OFF_K + bx * kBox, &p.tm_k, 64 * bx, row, fb);
-                            ptx::tma_load_2d(sbase + C::OFF_V + bx * kBox, &p.tm_v, 64 * bx, row, fb);
+                            ptx::tma_load_3d(sbase + C::OFF_K + bx * kBox, &p.tm_k, 64 * bx, v.kv * 128, hk, fb);
+                            ptx::tma_load_3d(sbase + C::OFF_V + bx * kBox, &p.tm_v, 64 * bx, v.kv * 128, hk, fb);
                         }
                         ++kvc;
                     }
-                    const int qrow = (v.b * p.Hq + v.hq) * p.S + v.q * 128;
+                    const int hqi = v.b * p.Hq + v.hq;
                     const int st = (int)(pc % C::kQStages);
                     if (q_armed[st] > 0 && !wait1(BAR(B_Q_EMPTY + st), (uint32_t)((q_armed[st] - 1) & 1), c,
                                                   kRoleProducer, (int)pc, 2)) {
@@ -252,7 +255,8 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                     ptx::mbar_arrive_expect_tx(fb, C::kQBytes);
                     const uint32_t sq = sbase + C::OFF_Q + st * C::kTile;
 #pragma unroll
-                    for (int bx = 0; bx < C::kNBox; ++bx) ptx::tma_load_2d(sq + bx * kBox, &p.tm_q, 64 * bx, qrow, fb);
+                    for (int bx = 0; bx < C::kNBox; ++bx)
+                        ptx::tma_load_3d(sq + bx * kBox, &p.tm_q, 64 * bx, v.q * 128, hqi, fb);
                     ++q_armed[st];
                     trace_ev<kProf>(p, pc, EV_PR_Q_ISSUED);
                     const int so = (int)(pc % C::kDoStages);
@@ -266,7 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                     const uint32_t sd = sbase + C::OFF_DO + so * C::kTile;
 #pragma unroll
                     for (int bx = 0; bx < C::kNBox; ++bx)
-                        ptx::tma_load_2d(sd + bx * kBox, &p.tm_do, 64 * bx, qrow, fb);
+                        ptx::tma_load_3d(sd + bx * kBox, &p.tm_do, 64 * bx, v.q * 128, hqi, fb);
                     ++do_armed[so];
                     trace_ev<kProf>(p, pc, EV_PR_DO_ISSUED);
                     ++pc;
@@ -404,17 +408,21 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
             const PairDesc d = descs[ds];
             if (d.flags & kEnd) break;
             // per-column statistics of this pair's Q tile: lane l holds columns c0+l and c0+32+l
-            const size_t qrow = (size_t)(d.b * p.Hq + d.hq) * p.S + (size_t)d.q * 128 + c0 + lane;
-            const float lse2_a = ptx::ld_nc(p.lse + qrow) * kLog2e;
-            const float lse2_b = ptx::ld_nc(p.lse + qrow + 32) * kLog2e;
-            const float delta_a = ptx::ld_nc(p.delta + qrow);
-            const float delta_b = ptx::ld_nc(p.delta + qrow + 32);
+            // (columns past S of a partial last tile read 0 and are masked)
+            const int qcol = d.q * 128 + c0 + lane;
+            const size_t qrow = (size_t)(d.b * p.Hq + d.hq) * p.S + (size_t)qcol;
+            const bool va = !kTail || qcol < p.S, vb = !kTail || qcol + 32 < p.S;
+            const float lse2_a = va ? ptx::ld_nc(p.lse + qrow) * kLog2e : 0.f;
+            const float lse2_b = vb ? ptx::ld_nc(p.lse + qrow + 32) * kLog2e : 0.f;
+            const float delta_a = va ? ptx::ld_nc(p.delta + qrow) : 0.f;
+            const float delta_b = vb ? ptx::ld_nc(p.delta + qrow + 32) : 0.f;
             if (!waitw(BAR(B_S_FULL), (uint32_t)(pp & 1), c, kRoleSoftmax, (int)pp, 1)) break;
             if (rec) trace_ev<kProf>(p, pp, EV_SM_S_SEEN);
             ptx::tc_fence_after();
             float P[64];
             unsigned long long tc0 = kProf ? clock64() : 0ull;
-            softmax_64(tmem + lane_off + C::COL_S, c0, lse2_a, lse2_b, p.scale_log2e, (d.flags & kDiag) != 0, row, P);
+            softmax_64<kTail || D == 64>(tmem + lane_off + C::COL_S, c0, lse2_a, lse2_b, p.scale_log2e, (d.flags & (kDiag | kPartial)) != 0,
+                       (d.flags & kDiag) != 0, row, p.S - d.kv * 128, p.S - d.q * 128, P);
             prof_add(c, kRoleSoftmax, 8, tc0);
             ptx::tc_fence_before();
             __syncwarp();
@@ -534,13 +542,17 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
             if (!ok) break;
             if (rec) trace_ev<kProf>(p, pp, EV_DR_TURN);
             float* gdq = p.dq + ((size_t)(d.b * p.Hq + d.hq) * p.S + (size_t)d.q * 128) * D;
+            const bool row_a = !kTail || d.q * 128 + qa < p.S;   // rows past S
+            const bool row_b = !kTail || d.q * 128 + qa + 8 < p.S;
             const int cofs = 2 * (lane & 2);
 #pragma unroll
             for (int j = 0; j < D / 8; j += 2) {
                 const int cb = 8 * (j + (odd ? 1 : 0)) + cofs;
-                ptx::red_add_v4(gdq + (size_t)qa * D + cb, __uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
-                                __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
-                ptx::red_add_v4(gdq + (size_t)(qa + 8) * D + cb, __uint_as_float(r[4 * (j + 1)]),
+                if (row_a)
+                    ptx::red_add_v4(gdq + (size_t)qa * D + cb, __uint_as_float(r[4 * j]), __uint_as_float(r[4 * j + 1]),
+                                    __uint_as_float(r[4 * j + 2]), __uint_as_float(r[4 * j + 3]));
+                if (row_b)
+                    ptx::red_add_v4(gdq + (size_t)(qa + 8) * D + cb, __uint_as_float(r[4 * (j + 1)]),
                                 __uint_as_float(r[4 * (j + 1) + 1]), __uint_as_float(r[4 * (j + 1) + 2]),
                                 __uint_as_float(r[4 * (j + 1) + 3]));
             }
@@ -557,6 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                 if (!waitw(BAR(B_ACC_FULL), (uint32_t)(kvc & 1), c, kRoleDrain, (int)pp, 2)) break;
                 ptx::tc_fence_after();
                 const int krow = 32 * sub + lane;
+                const bool krow_ok = !kTail || d.kv * 128 + krow < p.S;   // rows past S are not stored
                 const size_t grow = ((size_t)(d.b * p.Hkv + d.hkv) * p.S + (size_t)d.kv * 128 + krow) * D;
                 __nv_bfloat16* out = (half == 0 ? p.dk : p.dv) + grow;
                 const uint32_t col = half == 0 ? C::COL_DK : C::COL_DV;
@@ -571,10 +584,12 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                         __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
                         pk[e] = *reinterpret_cast<uint32_t*>(&h2);
                     }
+                    if (krow_ok) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        *reinterpret_cast<uint4*>(out + 32 * cc + 8 * e) =
-                            make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                        for (int e = 0; e < 4; ++e)
+                            *reinterpret_cast<uint4*>(out + 32 * cc + 8 * e) =
+                                make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                    }
                 }
                 ptx::tc_fence_before();
                 __syncwarp();
@@ -598,14 +613,14 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
     }
 }
 
-template <int D, bool kProf>
+template <int D, bool kProf, bool kTail>
 int launch_bwd(const BwdParams& prm, int grid, cudaStream_t stream) {
     using C = Cfg<D>;
     static bool attr_done[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -2;
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(dash_bwd_kernel<D, kProf>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(dash_bwd_kernel<D, kProf, kTail>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmem) != cudaSuccess)
             return -2;
         attr_done[dev] = true;
@@ -615,12 +630,12 @@ int launch_bwd(const BwdParams& prm, int grid, cudaStream_t stream) {
     static int regs_ok[64] = {};
     if (dev >= 0 && dev < 64 && regs_ok[dev] == 0) {
         cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, dash_bwd_kernel<D, kProf>) != cudaSuccess) return -2;
+        if (cudaFuncGetAttributes(&fa, dash_bwd_kernel<D, kProf, kTail>) != cudaSuccess) return -2;
         regs_ok[dev] = (fa.numRegs >= kRegsLaunch) ? 1 : -1;
     }
     if (dev < 0 || dev >= 64 || regs_ok[dev] != 1) return -3;
     void* args[] = {(void*)&prm};
-    cudaError_t e = cudaLaunchCooperativeKernel((const void*)dash_bwd_kernel<D, kProf>, dim3(grid),
+    cudaError_t e = cudaLaunchCooperativeKernel((const void*)dash_bwd_kernel<D, kProf, kTail>, dim3(grid),
                                                 dim3(kThreads), args, C::kSmem, stream);
     if (e == cudaErrorCooperativeLaunchTooLarge) {
         (void)cudaGetLastError();
@@ -635,14 +650,14 @@ int bwd_max_ctas(int D, int device, int* P) {
     int per_sm = 0;
     cudaError_t e;
     if (D == 64) {
-        cudaFuncSetAttribute(dash_bwd_kernel<64, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(dash_bwd_kernel<64, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg<64>::kSmem);
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dash_bwd_kernel<64, false>, kThreads,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dash_bwd_kernel<64, false, false>, kThreads,
                                                           Cfg<64>::kSmem);
     } else {
-        cudaFuncSetAttribute(dash_bwd_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(dash_bwd_kernel<128, false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              Cfg<128>::kSmem);
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dash_bwd_kernel<128, false>, kThreads,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dash_bwd_kernel<128, false, false>, kThreads,
                                                           Cfg<128>::kSmem);
     }
     if (e != cudaSuccess) return -2;
@@ -652,9 +667,14 @@ int bwd_max_ctas(int D, int device, int* P) {
 }
 
 int launch_bwd_dispatch(int D, const BwdParams& prm, int grid, cudaStream_t stream) {
+    if (prm.S % 128) {   // a partial last tile: the masked instantiation
+        if (prm.prof)
+            return D == 64 ? launch_bwd<64, true, true>(prm, grid, stream) : launch_bwd<128, true, true>(prm, grid, stream);
+        return D == 64 ? launch_bwd<64, false, true>(prm, grid, stream) : launch_bwd<128, false, true>(prm, grid, stream);
+    }
     if (prm.prof)
-        return D == 64 ? launch_bwd<64, true>(prm, grid, stream) : launch_bwd<128, true>(prm, grid, stream);
-    return D == 64 ? launch_bwd<64, false>(prm, grid, stream) : launch_bwd<128, false>(prm, grid, stream);
+        return D == 64 ? launch_bwd<64, true, false>(prm, grid, stream) : launch_bwd<128, true, false>(prm, grid, stream);
+    return D == 64 ? launch_bwd<64, false, false>(prm, grid, stream) : launch_bwd<128, false, false>(prm, grid, stream);
 }
 
 int bwd_smem_bytes(int D) { return D == 64 ? Cfg<64>::kSmem : Cfg<128>::kSmem; }

@@ -65,7 +65,8 @@ constexpr int kNDesc = 8;          // pair-descriptor ring depth
 constexpr float kLog2e = 1.4426950408889634f;
 
 enum Role : int { kRoleDrain = 0, kRoleProducer = 1, kRoleMma = 2, kRoleSoftmax = 3 };
-enum DescFlags : int { kKvFirst = 1, kKvLast = 2, kDiag = 4, kEnd = 8 };
+// kPartial: the pair touches the partial last tile (S % 128 != 0) in KV or Q.
+enum DescFlags : int { kKvFirst = 1, kKvLast = 2, kDiag = 4, kEnd = 8, kPartial = 16 };
 
 // Barrier slots (8 bytes each) at the start of the control area.
 enum Bar : int {
@@ -150,7 +151,7 @@ struct Regs {
 };
 
 struct BwdParams {
-    CUtensorMap tm_q, tm_k, tm_v, tm_do;   // 2D [rows, D] bf16, box 64 x 128, SWIZZLE_128B
+    CUtensorMap tm_q, tm_k, tm_v, tm_do;   // 3D [heads][S][D] bf16, box 64 x 128 x 1, SWIZZLE_128B
     const float* lse;
     const float* delta;
     float* dq;
@@ -235,8 +236,16 @@ __device__ __forceinline__ void issue_dq(uint32_t d_tmem, uint32_t sDsT, uint32_
 // bf16 P^T back into tensor memory at columns [c0, c0+32) of its own
 // 64-column span (so the MMA reads it as a K-major A operand).  lse2_* are
 // LSE * log2(e).  Works in 32-column halves to keep few registers live.
+// P is zero where row > column on a diagonal tile (`diag`) and, when `mask`
+// is set, where row >= lim_row (keys past S) or column >= lim_col (queries
+// past S).  kBranchMask: apply the masks in a branch taken only by masked
+// pairs (needed for partial tiles; measured faster at D = 64); otherwise the
+// diagonal is applied with a per-element select (measured faster at D = 128
+// and then lim_row, lim_col must be >= 128).
+template <bool kBranchMask>
 __device__ __forceinline__ void softmax_64(uint32_t tmem_s_lane, int c0, float lse2_a, float lse2_b,
-                                           float scale_log2e, bool diag, int row, float (&P)[64]) {
+                                           float scale_log2e, bool mask, bool diag, int row, int lim_row,
+                                           int lim_col, float (&P)[64]) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         uint32_t r[32];
@@ -247,7 +256,14 @@ __device__ __forceinline__ void softmax_64(uint32_t tmem_s_lane, int c0, float l
         for (int k = 0; k < 32; ++k) {
             const float l = __shfl_sync(0xffffffffu, lsrc, k);
             const float x = ptx::ex2(fmaf(__uint_as_float(r[k]), scale_log2e, -l));
-            P[32 * h + k] = (diag && row > c0 + 32 * h + k) ? 0.f : x;
+            P[32 * h + k] = (!kBranchMask && diag && row > c0 + 32 * h + k) ? 0.f : x;
+        }
+        if (kBranchMask && mask) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                const int col = c0 + 32 * h + k;
+                if ((diag && row > col) || row >= lim_row || col >= lim_col) P[32 * h + k] = 0.f;
+            }
         }
         uint32_t pk[16];
 #pragma unroll

@@ -38,7 +38,7 @@ namespace dash {
 namespace {
 
 struct FwdParams {
-    CUtensorMap tm_q, tm_k, tm_v;   // 2D [rows, D] bf16, box 64 x 128, SWIZZLE_128B
+    CUtensorMap tm_q, tm_k, tm_v;   // 3D [heads][S][D] bf16, box 64 x 128 x 1, SWIZZLE_128B
     __nv_bfloat16* o;
     float* lse;
     int* status;                    // [8]: code, info[4]
@@ -119,7 +119,9 @@ __device__ bool fwaitw(uint32_t bar, uint32_t parity, const FwdWait& w, int role
     return ok != 0;
 }
 
-template <int D>
+// kTail: compiled for S % 128 != 0 (masks and guards of the partial last
+// tile); the instantiation for whole tiles carries none of that code.
+template <int D, bool kTail>
 __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant__ FwdParams p) {
     using C = FwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -140,8 +142,8 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
     const int bh = (int)(blockIdx.x / p.n);
     const int b = bh / p.Hq, hq = bh % p.Hq, hkv = hq / p.G;
     const int nkv = p.causal ? qt + 1 : p.n;
-    const int qrow = (b * p.Hq + hq) * p.S + qt * 128;
-    const int kvrow0 = (b * p.Hkv + hkv) * p.S;
+    const int qrow = (b * p.Hq + hq) * p.S + qt * 128;   // first row of this tile in o / lse
+    const int hqi = b * p.Hq + hq, hki = b * p.Hkv + hkv;  // head indices of the 3-D tensor maps
 
     if (threadIdx.x == 0) {
         *abort_smem = (sbase & 1023u) ? 1 : 0;
@@ -177,22 +179,21 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
             ptx::mbar_arrive_expect_tx(BAR(F_Q_FULL), C::kTile);
 #pragma unroll
             for (int bx = 0; bx < C::kNBox; ++bx)
-                ptx::tma_load_2d(sbase + C::OFF_Q + bx * kBox, &p.tm_q, 64 * bx, qrow, BAR(F_Q_FULL));
+                ptx::tma_load_3d(sbase + C::OFF_Q + bx * kBox, &p.tm_q, 64 * bx, qt * 128, hqi, BAR(F_Q_FULL));
             int issued = 0;
             for (int j = 0; j < nkv; ++j) {
                 const int st = j & 1;
                 if (j >= 2 && !fwait1(BAR(F_K_EMPTY + st), (uint32_t)((j / 2 - 1) & 1), fw, 1, j)) break;
-                const int row = kvrow0 + j * 128;
                 ptx::mbar_arrive_expect_tx(BAR(F_K_FULL + st), C::kTile);
 #pragma unroll
                 for (int bx = 0; bx < C::kNBox; ++bx)
-                    ptx::tma_load_2d(sbase + C::OFF_K + st * C::kTile + bx * kBox, &p.tm_k, 64 * bx, row,
+                    ptx::tma_load_3d(sbase + C::OFF_K + st * C::kTile + bx * kBox, &p.tm_k, 64 * bx, j * 128, hki,
                                      BAR(F_K_FULL + st));
                 if (j >= 2 && !fwait1(BAR(F_V_EMPTY + st), (uint32_t)((j / 2 - 1) & 1), fw, 1, j)) break;
                 ptx::mbar_arrive_expect_tx(BAR(F_V_FULL + st), C::kTile);
 #pragma unroll
                 for (int bx = 0; bx < C::kNBox; ++bx)
-                    ptx::tma_load_2d(sbase + C::OFF_V + st * C::kTile + bx * kBox, &p.tm_v, 64 * bx, row,
+                    ptx::tma_load_3d(sbase + C::OFF_V + st * C::kTile + bx * kBox, &p.tm_v, 64 * bx, j * 128, hki,
                                      BAR(F_V_FULL + st));
                 issued = j + 1;
             }
@@ -274,6 +275,12 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
                 for (int k = 0; k < 128; ++k)
                     if (k > row) x[k] = -INFINITY;
             }
+            if (kTail && j == p.n - 1) {   // keys past S of the partial last tile
+                const int lim = p.S - j * 128;
+#pragma unroll
+                for (int k = 0; k < 128; ++k)
+                    if (k >= lim) x[k] = -INFINITY;
+            }
             // row max and (below) row sum over 8 interleaved partials: short
             // dependency chains, and a fixed order of the additions
             float part[8];
@@ -340,6 +347,7 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
             ok = fwaitw(BAR(F_O_DONE), (uint32_t)(jj & 1), fw, 3, nkv);
         if (ok) {
             ptx::tc_fence_after();
+            const bool row_ok = !kTail || qt * 128 + row < p.S;   // rows past S are not stored (loads stay warp-wide)
             const float inv = 1.f / l;
             __nv_bfloat16* orow = p.o + ((size_t)qrow + row) * D;
 #pragma unroll
@@ -354,12 +362,14 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
                         __floats2bfloat162_rn(__uint_as_float(r[2 * k]) * inv, __uint_as_float(r[2 * k + 1]) * inv);
                     pk[k] = *reinterpret_cast<uint32_t*>(&h2);
                 }
+                if (row_ok) {
 #pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    *reinterpret_cast<uint4*>(orow + 32 * cc + 8 * e) =
-                        make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                    for (int e = 0; e < 4; ++e)
+                        *reinterpret_cast<uint4*>(orow + 32 * cc + 8 * e) =
+                            make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                }
             }
-            p.lse[qrow + row] = (m_ref + log2f(l)) * kLn2;
+            if (row_ok) p.lse[qrow + row] = (m_ref + log2f(l)) * kLn2;
         }
     }
 
@@ -371,18 +381,18 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
     }
 }
 
-template <int D>
+template <int D, bool kTail>
 int launch_fwd_t(const FwdParams& prm, int grid, cudaStream_t stream) {
     static bool attr_done[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -2;
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(dash_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(dash_fwd_kernel<D, kTail>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  FwdCfg<D>::kSmem) != cudaSuccess)
             return -2;
         attr_done[dev] = true;
     }
-    dash_fwd_kernel<D><<<grid, 256, FwdCfg<D>::kSmem, stream>>>(prm);
+    dash_fwd_kernel<D, kTail><<<grid, 256, FwdCfg<D>::kSmem, stream>>>(prm);
     return cudaGetLastError() == cudaSuccess ? 0 : -2;
 }
 
@@ -391,8 +401,8 @@ int launch_fwd_t(const FwdParams& prm, int grid, cudaStream_t stream) {
 int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int* status, int B, int Hq,
                int Hkv, int S, int D, int causal, unsigned long long timeout_ns, cudaStream_t stream) {
     FwdParams prm;
-    if (make_tmap_2d(&prm.tm_q, q, (long long)B * Hq * S, D) || make_tmap_2d(&prm.tm_k, k, (long long)B * Hkv * S, D) ||
-        make_tmap_2d(&prm.tm_v, v, (long long)B * Hkv * S, D))
+    if (make_tmap_3d(&prm.tm_q, q, (long long)B * Hq, S, D) || make_tmap_3d(&prm.tm_k, k, (long long)B * Hkv, S, D) ||
+        make_tmap_3d(&prm.tm_v, v, (long long)B * Hkv, S, D))
         return -2;
     prm.o = (__nv_bfloat16*)o;
     prm.lse = lse;
@@ -402,13 +412,15 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
     prm.Hq = Hq;
     prm.Hkv = Hkv;
     prm.S = S;
-    prm.n = S / 128;
+    prm.n = (S + 127) / 128;   // the last tile may be partial
     prm.G = Hq / Hkv;
     prm.causal = causal;
     prm.scale_log2e = (1.0f / sqrtf((float)D)) * kLog2e;
-    const long long grid = (long long)B * Hq * (S / 128);
+    const long long grid = (long long)B * Hq * ((S + 127) / 128);
     if (grid <= 0 || grid > 0x7fffffffll) return -1;
-    return D == 64 ? launch_fwd_t<64>(prm, (int)grid, stream) : launch_fwd_t<128>(prm, (int)grid, stream);
+    if (S % 128)
+        return D == 64 ? launch_fwd_t<64, true>(prm, (int)grid, stream) : launch_fwd_t<128, true>(prm, (int)grid, stream);
+    return D == 64 ? launch_fwd_t<64, false>(prm, (int)grid, stream) : launch_fwd_t<128, false>(prm, (int)grid, stream);
 }
 
 }  // namespace dash

@@ -33,6 +33,7 @@ int run_tile_probe(const void* k, const void* v, const void* q, const void* dO, 
 
 // Tensor maps (dash_api.cu).
 int make_tmap_2d(void* map_out, const void* base, long long rows, int D);
+int make_tmap_3d(void* map_out, const void* base, long long heads, int S, int D);
 int make_tmap_2d_f32(void* map_out, const void* base, long long rows, int D);
 
 }  // namespace dash

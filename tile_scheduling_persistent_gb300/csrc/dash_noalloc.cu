@@ -70,8 +70,9 @@ extern "C" int dash_attn_bwd_noalloc(const dash_bf16* q, const dash_bf16* k, con
     const void* ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv};
     for (const void* ptr : ptrs)
         if (!ptr || ((uintptr_t)ptr & 15u)) return DASH_ERR_ARG;
-    if (B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 || S % 128 || (D != 64 && D != 128) || Hq % Hkv ||
-        (causal != 0 && causal != 1) || schedule < 0 || schedule > kAuto || (long long)B * Hq * S >= (1ll << 31))
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || S <= 0 || (D != 64 && D != 128) || Hq % Hkv ||
+        (causal != 0 && causal != 1) || schedule < 0 || schedule > kAuto || (long long)B * Hq * S >= (1ll << 31) ||
+        (S + 127) / 128 > 65535)
         return DASH_ERR_ARG;
     if (schedule == kAuto) schedule = select_schedule(D, causal);
     int dev = 0, major = 0, minor = 0;
@@ -85,7 +86,7 @@ extern "C" int dash_attn_bwd_noalloc(const dash_bf16* q, const dash_bf16* k, con
     if (rc == -3) return DASH_ERR_LAUNCH;
     if (rc) return DASH_ERR_CUDA;
 
-    const int n = S / 128;
+    const int n = (S + 127) / 128;   // the last tile may be partial
     const Shape sh{B, Hq, Hkv, n, Hq / Hkv, causal, schedule};
     const long long tiles = (long long)B * Hq * n;
     const long long entries = tiles * n;
@@ -113,14 +114,14 @@ extern "C" int dash_attn_bwd_noalloc(const dash_bf16* q, const dash_bf16* k, con
                                      reinterpret_cast<uint32_t*>(base + off_start), stream))
         return DASH_ERR_CUDA;
     if (cudaMemsetAsync(ints, 0, n_ints * sizeof(int), stream) != cudaSuccess ||
-        cudaMemsetAsync(dq, 0, (size_t)tiles * 128 * D * sizeof(float), stream) != cudaSuccess)
+        cudaMemsetAsync(dq, 0, (size_t)B * Hq * S * D * sizeof(float), stream) != cudaSuccess)
         return DASH_ERR_CUDA;
-    if (launch_preprocess(o, dO, delta, tiles * 128, D, stream)) return DASH_ERR_CUDA;
+    if (launch_preprocess(o, dO, delta, (long long)B * Hq * S, D, stream)) return DASH_ERR_CUDA;
 
     BwdParams prm;
     memset(&prm, 0, sizeof(prm));
-    if (make_tmap_2d(&prm.tm_q, q, (long long)B * Hq * S, D) || make_tmap_2d(&prm.tm_k, k, (long long)B * Hkv * S, D) ||
-        make_tmap_2d(&prm.tm_v, v, (long long)B * Hkv * S, D) || make_tmap_2d(&prm.tm_do, dO, (long long)B * Hq * S, D))
+    if (make_tmap_3d(&prm.tm_q, q, (long long)B * Hq, S, D) || make_tmap_3d(&prm.tm_k, k, (long long)B * Hkv, S, D) ||
+        make_tmap_3d(&prm.tm_v, v, (long long)B * Hkv, S, D) || make_tmap_3d(&prm.tm_do, dO, (long long)B * Hq, S, D))
         return DASH_ERR_CUDA;
     prm.lse = lse;
     prm.delta = delta;
