@@ -242,6 +242,17 @@ int dash_sim_schedule(int schedule, int causal, int B, int Hq, int Hkv, int n, i
                       int64_t* num_tasks);
 
 /*
+ * dash_sim_schedule_band -- dash_sim_schedule for a causal sliding window
+ * that touches `band` tile diagonals (tile pair (q, kv) visited iff
+ * 0 <= q - kv < band; band >= 1).  The tiles outside the band are skipped the
+ * way the masked tiles of a causal mask are; symmetric shift is shift there.
+ * Same outputs and errors as dash_sim_schedule.
+ */
+int dash_sim_schedule_band(int schedule, int B, int Hq, int Hkv, int n, int band, int P,
+                           double c, double r, double* makespan, int32_t* turn_order,
+                           int64_t* num_tasks);
+
+/*
  * dash_sim_check_ranks -- would the kernel complete with this accumulation
  * table?  ranks: host uint16 [B*Hq*n][n], rank of KV tile j's partial in dQ
  * tile i (entries of masked pairs are ignored).  The visit lists and SM

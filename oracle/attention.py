@@ -16,6 +16,7 @@ batch ``b`` and query head ``hq`` (key/value head ``hk = hq // (Hq // Hkv)``):
 
     s_ij  = scale * <q_i, k_j>                       scale = 1 / sqrt(D)
     allowed(i, j) = (j <= i) if causal else True      (top-left causal mask)
+                    and, with a sliding window of W tokens, i - j < W
     L_i   = log sum_{j allowed} exp(s_ij)             natural log
     p_ij  = exp(s_ij - L_i)  (0 where not allowed)
     O_i   = sum_j p_ij v_j
@@ -25,6 +26,11 @@ batch ``b`` and query head ``hq`` (key/value head ``hk = hq // (Hq // Hkv)``):
     dQ_i  = scale * sum_j ds_ij k_j
     dK_j  = sum over the heads hq of group hk, ascending, of scale * sum_i ds_ij q_i
     dV_j  = sum over the heads hq of group hk, ascending, of sum_i p_ij dO_i
+
+The sliding window (``window=W``, causal masks only) is the band mask of the
+Ascend plan (ocdem.com, section 2.3.5: lower-triangular and band masks, with
+tiles that are entirely masked skipped): key j is visible to query i iff
+i - W < j <= i.  W >= S is the plain causal mask.
 
 Everything is float64.  ``attn_bwd`` takes O and LSE as arguments, so the
 same code gives the graded variant (exact fp64 O/LSE from ``attn_fwd``) and
@@ -68,11 +74,21 @@ def _scale(D: int, scale: float | None) -> float:
     return 1.0 / math.sqrt(D) if scale is None else float(scale)
 
 
-def _allowed(rows: np.ndarray, S: int, causal: bool) -> np.ndarray | None:
-    """Boolean mask [len(rows), S]: key j is visible to query i iff j <= i."""
+def _check_window(causal: bool, window):
+    if window is not None and (not causal or int(window) < 1):
+        raise ValueError("a sliding window needs a causal mask and window >= 1")
+
+
+def _allowed(rows: np.ndarray, S: int, causal: bool, window=None) -> np.ndarray | None:
+    """Boolean mask [len(rows), S]: key j is visible to query i iff j <= i
+    (and i - j < window)."""
     if not causal:
         return None
-    return np.arange(S)[None, :] <= rows[:, None]
+    j = np.arange(S)[None, :]
+    ok = j <= rows[:, None]
+    if window is not None:
+        ok &= rows[:, None] - j < int(window)
+    return ok
 
 
 def _row_blocks(S: int, row_block: int | None):
@@ -81,14 +97,14 @@ def _row_blocks(S: int, row_block: int | None):
         yield r0, min(S, r0 + step)
 
 
-def _fwd_head(qh, kh, vh, causal, scale, row_block):
+def _fwd_head(qh, kh, vh, causal, scale, row_block, window=None):
     S = qh.shape[0]
     O = np.empty_like(qh)
     L = np.empty(S, dtype=np.float64)
     for r0, r1 in _row_blocks(S, row_block):
         rows = np.arange(r0, r1)
         s = scale * (qh[r0:r1] @ kh.T)
-        allowed = _allowed(rows, kh.shape[0], causal)
+        allowed = _allowed(rows, kh.shape[0], causal, window)
         if allowed is not None:
             s = np.where(allowed, s, -np.inf)
         m = s.max(axis=1)
@@ -101,8 +117,9 @@ def _fwd_head(qh, kh, vh, causal, scale, row_block):
 
 
 def attn_fwd(q, k, v, causal: bool, scale: float | None = None,
-             row_block: int | None = None, workers: int = 1):
+             row_block: int | None = None, workers: int = 1, window: int | None = None):
     """Exact fp64 forward: returns (O [B,Hq,S,D], LSE [B,Hq,S])."""
+    _check_window(causal, window)
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, Hq, S, D = q.shape
     Hkv = k.shape[1]
@@ -114,7 +131,7 @@ def attn_fwd(q, k, v, causal: bool, scale: float | None = None,
     def one(bh):
         b, hq = divmod(bh, Hq)
         hk = hq // G
-        O[b, hq], L[b, hq] = _fwd_head(q[b, hq], k[b, hk], v[b, hk], causal, sc, row_block)
+        O[b, hq], L[b, hq] = _fwd_head(q[b, hq], k[b, hk], v[b, hk], causal, sc, row_block, window)
 
     _run(one, B * Hq, workers)
     return O, L
@@ -125,7 +142,7 @@ def attn_bwd_delta(o, do) -> np.ndarray:
     return np.einsum("bhsd,bhsd->bhs", _f64(do), _f64(o))
 
 
-def _bwd_head(qh, kh, vh, doh, lseh, deltah, causal, scale, row_block):
+def _bwd_head(qh, kh, vh, doh, lseh, deltah, causal, scale, row_block, window=None):
     S, D = qh.shape
     dq = np.empty_like(qh)
     dk = np.zeros_like(kh)
@@ -134,7 +151,7 @@ def _bwd_head(qh, kh, vh, doh, lseh, deltah, causal, scale, row_block):
         rows = np.arange(r0, r1)
         s = scale * (qh[r0:r1] @ kh.T)
         p = np.exp(s - lseh[r0:r1, None])
-        allowed = _allowed(rows, kh.shape[0], causal)
+        allowed = _allowed(rows, kh.shape[0], causal, window)
         if allowed is not None:
             p = np.where(allowed, p, 0.0)
         dp = doh[r0:r1] @ vh.T
@@ -146,7 +163,7 @@ def _bwd_head(qh, kh, vh, doh, lseh, deltah, causal, scale, row_block):
 
 
 def attn_bwd(q, k, v, o, do, lse, causal: bool, scale: float | None = None,
-             row_block: int | None = None, workers: int = 1):
+             row_block: int | None = None, workers: int = 1, window: int | None = None):
     """fp64 backward.  Returns (dq, dk, dv, delta).
 
     ``o`` and ``lse`` are taken as given (exact from ``attn_fwd`` for the
@@ -154,6 +171,7 @@ def attn_bwd(q, k, v, o, do, lse, causal: bool, scale: float | None = None,
     one).  dK and dV of a key/value head are the sum of the per-query-head
     contributions of its group, added in ascending query-head order.
     """
+    _check_window(causal, window)
     q, k, v, o, do, lse = (_f64(x) for x in (q, k, v, o, do, lse))
     B, Hq, S, D = q.shape
     Hkv = k.shape[1]
@@ -169,7 +187,7 @@ def attn_bwd(q, k, v, o, do, lse, causal: bool, scale: float | None = None,
         hk = hq // G
         dq[b, hq], part_k[b, hq], part_v[b, hq] = _bwd_head(
             q[b, hq], k[b, hk], v[b, hk], do[b, hq], lse[b, hq], delta[b, hq],
-            causal, sc, row_block)
+            causal, sc, row_block, window)
 
     _run(one, B * Hq, workers)
     dk = np.zeros_like(k)
@@ -180,7 +198,7 @@ def attn_bwd(q, k, v, o, do, lse, causal: bool, scale: float | None = None,
     return dq, dk, dv, delta
 
 
-def dq_rows(q, k, v, o, do, lse, causal, b, hq, rows, scale=None):
+def dq_rows(q, k, v, o, do, lse, causal, b, hq, rows, scale=None, window=None):
     """dQ for selected query rows of one head, one row at a time (fp64).
 
     Same definition as ``attn_bwd``; cost O(S*D) per row, so it can sample
@@ -197,6 +215,8 @@ def dq_rows(q, k, v, o, do, lse, causal, b, hq, rows, scale=None):
         p = np.exp(s - lse[b, hq, i])
         if causal:
             p[i + 1:] = 0.0
+        if window is not None:
+            p[:max(0, i - int(window) + 1)] = 0.0
         dp = V @ do[b, hq, i]
         delta = do[b, hq, i] @ o[b, hq, i]
         ds = p * (dp - delta)
@@ -204,7 +224,7 @@ def dq_rows(q, k, v, o, do, lse, causal, b, hq, rows, scale=None):
     return out
 
 
-def dkv_rows(q, k, v, o, do, lse, causal, b, hk, rows, scale=None):
+def dkv_rows(q, k, v, o, do, lse, causal, b, hk, rows, scale=None, window=None):
     """dK and dV for selected key rows of one key/value head (fp64).
 
     Sums the contributions of every query head of the group in ascending
@@ -224,6 +244,8 @@ def dkv_rows(q, k, v, o, do, lse, causal, b, hk, rows, scale=None):
             p = np.exp(s - lse[b, hq])
             if causal:
                 p[:j] = 0.0
+            if window is not None:
+                p[j + int(window):] = 0.0
             dp = dO @ v[b, hk, j]
             ds = p * (dp - delta)
             dk[n] += sc * (ds @ Q)
@@ -231,8 +253,12 @@ def dkv_rows(q, k, v, o, do, lse, causal, b, hk, rows, scale=None):
     return dk, dv
 
 
-def flops_nominal(B: int, Hq: int, S: int, D: int, causal: bool) -> float:
-    """Nominal backward FLOPs: 10*S^2*D per query head, halved for causal."""
+def flops_nominal(B: int, Hq: int, S: int, D: int, causal: bool, window: int | None = None) -> float:
+    """Nominal backward FLOPs: 10*D per visible (query, key) pair per query
+    head, counted as S^2 (full), S^2/2 (causal) or S*W - W^2/2 (sliding
+    window W <= S)."""
+    if window is not None and window < S:
+        return 10.0 * D * B * Hq * (S * window - window * window / 2.0)
     f = 10.0 * S * S * D * B * Hq
     return f / 2 if causal else f
 

@@ -100,19 +100,37 @@ class SimResult:
 # visit lists
 # --------------------------------------------------------------------------
 
-def _allowed(i: int, j: int, causal: bool) -> bool:
-    return (not causal) or j <= i
+def band_tiles(window: int, tile: int = 128) -> int:
+    """Number of tile diagonals a causal sliding window of `window` tokens
+    touches: tile pair (i, j) holds a visible (query, key) element iff
+    0 <= i - j < band_tiles(window).  Diagonal t >= 1 holds one iff its
+    smallest query-key distance, tile * t - (tile - 1), is below the window."""
+    t = 1
+    while tile * t - (tile - 1) < window:
+        t += 1
+    return t
 
 
-def visit_q(schedule: str, n: int, causal: bool, j: int) -> list:
-    """Q tiles visited by KV tile j, in order (non-symmetric schedules)."""
+def _allowed(i: int, j: int, causal: bool, band=None) -> bool:
+    if not causal:
+        return True
+    return j <= i and (band is None or i - j < band)
+
+
+def visit_q(schedule: str, n: int, causal: bool, j: int, band=None) -> list:
+    """Q tiles visited by KV tile j, in order (non-symmetric schedules).
+
+    With a band (sliding window), tiles outside it are skipped as the
+    masked tiles of a causal mask are; symmetric shift is then read as shift
+    (all tasks but the last few have the same length, so there is no
+    triangle to fold)."""
     if schedule in ("serialized_ascending", "atomic_nondet"):
-        return [i for i in range(n) if _allowed(i, j, causal)]
+        return [i for i in range(n) if _allowed(i, j, causal, band)]
     if schedule == "descending_q":
-        return [i for i in reversed(range(n)) if _allowed(i, j, causal)]
-    if schedule == "shift" or (schedule == "symmetric_shift" and not causal):
+        return [i for i in reversed(range(n)) if _allowed(i, j, causal, band)]
+    if schedule == "shift" or (schedule == "symmetric_shift" and (not causal or band is not None)):
         rot = [(j + t) % n for t in range(n)]
-        return [i for i in rot if _allowed(i, j, causal)]
+        return [i for i in rot if _allowed(i, j, causal, band)]
     raise ValueError(schedule)
 
 
@@ -132,7 +150,7 @@ def symmetric_task(n: int, jp: int):
     return a, b
 
 
-def make_tasks(schedule: str, B: int, Hq: int, Hkv: int, n: int, causal: bool) -> list:
+def make_tasks(schedule: str, B: int, Hq: int, Hkv: int, n: int, causal: bool, band=None) -> list:
     """All tasks in dispatch order; each task is a list of Pair in run order."""
     if schedule not in SCHEDULES:
         raise ValueError(schedule)
@@ -141,7 +159,7 @@ def make_tasks(schedule: str, B: int, Hq: int, Hkv: int, n: int, causal: bool) -
     for b in range(B):
         for hk in range(Hkv):
             heads = range(hk * G, (hk + 1) * G)
-            if schedule == "symmetric_shift" and causal:
+            if schedule == "symmetric_shift" and causal and band is None:
                 for jp in range((n + 1) // 2):
                     a, bb = symmetric_task(n, jp)
                     t = [Pair(b, hq, i, kv) for hq in heads for (kv, i) in a]
@@ -150,13 +168,16 @@ def make_tasks(schedule: str, B: int, Hq: int, Hkv: int, n: int, causal: bool) -
             else:
                 for j in range(n):
                     tasks.append([Pair(b, hq, i, j) for hq in heads
-                                  for i in visit_q(schedule, n, causal, j)])
+                                  for i in visit_q(schedule, n, causal, j, band)])
     return tasks
 
 
-def build(schedule: str, B: int, Hq: int, Hkv: int, n: int, causal: bool, P: int) -> Schedule:
-    """Tasks, assignment and accumulation order of a schedule."""
-    tasks = make_tasks(schedule, B, Hq, Hkv, n, causal)
+def build(schedule: str, B: int, Hq: int, Hkv: int, n: int, causal: bool, P: int, band=None) -> Schedule:
+    """Tasks, assignment and accumulation order of a schedule (band: tile
+    diagonals of a sliding window, from band_tiles, or None)."""
+    if band is not None and (not causal or band < 1):
+        raise ValueError("a band needs a causal mask and band >= 1")
+    tasks = make_tasks(schedule, B, Hq, Hkv, n, causal, band)
     static = schedule in STATIC
     s = Schedule(schedule, B, Hq, Hkv, n, causal, P, tasks, static)
     if static:

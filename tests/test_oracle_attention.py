@@ -195,11 +195,11 @@ def test_flops_nominal():
 
 # ---- planted mistakes: each must be caught by the finite-difference pin ----
 
-def _mut_no_delta(qh, kh, vh, doh, lseh, deltah, causal, scale, row_block):
+def _mut_no_delta(qh, kh, vh, doh, lseh, deltah, causal, scale, row_block, window=None):
     return _orig_bwd_head(qh, kh, vh, doh, lseh, np.zeros_like(deltah), causal, scale, row_block)
 
 
-def _mut_transposed_dk(qh, kh, vh, doh, lseh, deltah, causal, scale, row_block):
+def _mut_transposed_dk(qh, kh, vh, doh, lseh, deltah, causal, scale, row_block, window=None):
     dq, dk, dv = _orig_bwd_head(qh, kh, vh, doh, lseh, deltah, causal, scale, row_block)
     # dK built from dS (not dS^T): equivalent to swapping the roles of i and j
     s = scale * qh @ kh.T
@@ -210,7 +210,7 @@ def _mut_transposed_dk(qh, kh, vh, doh, lseh, deltah, causal, scale, row_block):
     return dq, scale * ds @ qh, dv
 
 
-def _mut_mask_off_by_one(qh, kh, vh, doh, lseh, deltah, causal, scale, row_block):
+def _mut_mask_off_by_one(qh, kh, vh, doh, lseh, deltah, causal, scale, row_block, window=None):
     S = qh.shape[0]
     s = scale * qh @ kh.T
     p = np.exp(s - lseh[:, None])
@@ -221,7 +221,7 @@ def _mut_mask_off_by_one(qh, kh, vh, doh, lseh, deltah, causal, scale, row_block
     return scale * ds @ kh, scale * ds.T @ qh, p.T @ doh
 
 
-def _mut_sign(qh, kh, vh, doh, lseh, deltah, causal, scale, row_block):
+def _mut_sign(qh, kh, vh, doh, lseh, deltah, causal, scale, row_block, window=None):
     dq, dk, dv = _orig_bwd_head(qh, kh, vh, doh, lseh, deltah, causal, scale, row_block)
     return -dq, dk, dv
 
@@ -234,3 +234,101 @@ _orig_bwd_head = A._bwd_head
 def test_planted_mistakes_are_caught(monkeypatch, mutant, causal):
     monkeypatch.setattr(A, "_bwd_head", mutant)
     assert check_fd(1, 2, 1, 8, 4, causal) > 1e-3
+
+
+def _mut_window_off_by_one(qh, kh, vh, doh, lseh, deltah, causal, scale, row_block, window=None):
+    # the band with one key too many (i - j <= W instead of < W)
+    return _orig_bwd_head(qh, kh, vh, doh, lseh, deltah, causal, scale, row_block,
+                          None if window is None else window + 1)
+
+
+def test_planted_window_mistake_is_caught(monkeypatch):
+    monkeypatch.setattr(A, "_bwd_head", _mut_window_off_by_one)
+    q, k, v, do = make(1, 2, 1, 16, 8, seed=11)
+    o, lse = A.attn_fwd(q, k, v, True, window=3)
+    dq, _, _, _ = A.attn_bwd(q, k, v, o, do, lse, True, window=3)
+    num = fd_grad(lambda: loss_w(q, k, v, do, 3), q)
+    assert rel_err(dq, num) > 1e-3
+
+
+# ---- the sliding window (causal band of W tokens: i - W < j <= i) ----
+
+def loss_w(q, k, v, do, window):
+    o, _ = A.attn_fwd(q, k, v, True, window=window)
+    return float(np.sum(o * do))
+
+
+@pytest.mark.parametrize("B,Hq,Hkv,S,D,window", [(1, 2, 1, 16, 8, 3), (2, 1, 1, 9, 4, 5), (1, 2, 2, 12, 4, 2)])
+def test_window_finite_differences(B, Hq, Hkv, S, D, window):
+    q, k, v, do = make(B, Hq, Hkv, S, D, seed=11)
+    o, lse = A.attn_fwd(q, k, v, True, window=window)
+    dq, dk, dv, _ = A.attn_bwd(q, k, v, o, do, lse, True, window=window)
+    f = lambda: loss_w(q, k, v, do, window)  # noqa: E731
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        assert rel_err(g, fd_grad(f, x)) <= 1e-6
+
+
+def test_window_at_least_s_is_causal():
+    q, k, v, do = make(1, 2, 1, 24, 8, seed=12)
+    o_c, l_c = A.attn_fwd(q, k, v, True)
+    for w in (24, 25, 1000):
+        o_w, l_w = A.attn_fwd(q, k, v, True, window=w)
+        assert np.array_equal(o_w, o_c) and np.array_equal(l_w, l_c)
+        g_c = A.attn_bwd(q, k, v, o_c, do, l_c, True)
+        g_w = A.attn_bwd(q, k, v, o_w, do, l_w, True, window=w)
+        for a, b in zip(g_c, g_w):
+            assert np.array_equal(a, b)
+
+
+def test_window_one_closed_form():
+    """W = 1: every query sees only its own key, so p = 1 on the diagonal,
+    O_i = v_i, LSE_i = scale <q_i, k_i>, dS = 1 * (<dO_i, v_i> - <dO_i, O_i>) = 0,
+    hence dQ = dK = 0 and dV_j = the group's sum of dO_j."""
+    B, Hq, Hkv, S, D = 2, 4, 2, 10, 8
+    q, k, v, do = make(B, Hq, Hkv, S, D, seed=13)
+    o, lse = A.attn_fwd(q, k, v, True, window=1)
+    G = Hq // Hkv
+    for hq in range(Hq):
+        np.testing.assert_allclose(o[:, hq], v[:, hq // G], atol=1e-14)
+        np.testing.assert_allclose(lse[:, hq], np.einsum("bsd,bsd->bs", q[:, hq], k[:, hq // G]) / math.sqrt(D),
+                                   atol=1e-13)
+    dq, dk, dv, _ = A.attn_bwd(q, k, v, o, do, lse, True, window=1)
+    assert np.abs(dq).max() < 1e-13 and np.abs(dk).max() < 1e-13
+    for hk in range(Hkv):
+        np.testing.assert_allclose(dv[:, hk], do[:, hk * G:(hk + 1) * G].sum(axis=1), atol=1e-13)
+
+
+def test_window_matches_torch_autograd_with_a_band_mask():
+    q, k, v, do = make(1, 4, 2, 40, 16, seed=14)
+    W, S, G = 7, 40, 2
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    s = tq @ tk.repeat_interleave(G, dim=1).transpose(-1, -2) / 4.0
+    i = torch.arange(S)[:, None]
+    j = torch.arange(S)[None, :]
+    s = s.masked_fill(~((j <= i) & (i - j < W)), float("-inf"))
+    o_t = torch.softmax(s, dim=-1) @ tv.repeat_interleave(G, dim=1)
+    (o_t * torch.tensor(do)).sum().backward()
+    o, lse = A.attn_fwd(q, k, v, True, window=W)
+    np.testing.assert_allclose(o, o_t.detach().numpy(), rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(lse, torch.logsumexp(s, dim=-1).detach().numpy(), rtol=1e-12, atol=1e-12)
+    dq, dk, dv, _ = A.attn_bwd(q, k, v, o, do, lse, True, window=W)
+    for a, b in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+        np.testing.assert_allclose(a, b.numpy(), rtol=1e-10, atol=1e-11)
+    r = [0, 5, 6, 7, 39]
+    np.testing.assert_allclose(A.dq_rows(q, k, v, o, do, lse, True, 0, 3, r, window=W), dq[0, 3, r], atol=1e-13)
+    dk_r, dv_r = A.dkv_rows(q, k, v, o, do, lse, True, 0, 1, r, window=W)
+    np.testing.assert_allclose(dk_r, dk[0, 1, r], atol=1e-13)
+    np.testing.assert_allclose(dv_r, dv[0, 1, r], atol=1e-13)
+
+
+def test_window_rejected_without_causal_mask():
+    q, k, v, _ = make(1, 1, 1, 4, 4, seed=15)
+    with pytest.raises(ValueError):
+        A.attn_fwd(q, k, v, False, window=2)
+    with pytest.raises(ValueError):
+        A.attn_fwd(q, k, v, True, window=0)
+
+
+def test_window_flops():
+    assert A.flops_nominal(1, 1, 1024, 64, True, window=256) == 10.0 * 64 * (1024 * 256 - 256 * 256 / 2)
+    assert A.flops_nominal(1, 1, 1024, 64, True, window=4096) == A.flops_nominal(1, 1, 1024, 64, True)

@@ -9,6 +9,7 @@ import itertools
 import os
 import random
 
+import numpy as np
 import pytest
 
 from oracle import dagsim as G
@@ -222,3 +223,28 @@ def test_static_turn_order_is_deadlock_free_at_any_P():
                 s = G.build(sched, 1, 4, 2, 6, causal, P)
                 seqs = [[p for k in s.cta_tasks[c] for p in s.tasks[k]] for c in range(P)]
                 assert G.check_tables(seqs, G.turn_ranks(s))
+
+
+def test_band_tiles_from_element_visibility():
+    """band_tiles(W) counts the tile diagonals that hold a visible element of
+    a causal W-token window, checked by brute force over the elements."""
+    T = 8   # a small tile makes the brute force cheap; the rule is the same for 128
+    for W in range(1, 40):
+        want = 0
+        for t in range(0, 8):
+            q = np.arange(T)[:, None] + T * t
+            k = np.arange(T)[None, :]
+            if ((q - k >= 0) & (q - k < W)).any():
+                want = t + 1
+        assert G.band_tiles(W, tile=T) == want, W
+    assert G.band_tiles(1) == 1 and G.band_tiles(128) == 2 and G.band_tiles(129) == 2 and G.band_tiles(130) == 3
+
+
+def test_band_wide_enough_is_causal():
+    for sched in G.SCHEDULES:
+        a = G.build(sched, 1, 2, 1, 6, True, 4)
+        b = G.build(sched, 1, 2, 1, 6, True, 4, band=6)
+        if sched == "symmetric_shift":
+            continue   # with a band it is read as shift
+        assert a.tasks == b.tasks
+        assert a.turn == b.turn

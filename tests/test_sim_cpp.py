@@ -101,3 +101,28 @@ def test_check_ranks(causal):
         seqs = [[p for k in seqs_model.cta_tasks[c] for p in seqs_model.tasks[k]] for c in range(P)]
         pr = {p: int(rev[(p.b * Hq + p.hq) * n + p.i, p.j]) for t in seqs_model.tasks for p in t}
         assert (verdict == dash.OK) == G.check_tables(seqs, pr)
+
+
+BAND_CASES = [(sched, B, Hq, Hkv, n, band, P)
+              for sched in G.SCHEDULES
+              for (B, Hq, Hkv, n, band, P) in [(1, 1, 1, 6, 1, 4), (1, 2, 2, 7, 2, 3), (2, 4, 2, 8, 3, 5),
+                                               (1, 4, 1, 9, 4, 7), (1, 2, 1, 5, 9, 16), (2, 2, 2, 6, 6, 1)]]
+
+
+@pytest.mark.parametrize("sched,B,Hq,Hkv,n,band,P", BAND_CASES)
+def test_cpp_matches_oracle_with_a_band(sched, B, Hq, Hkv, n, band, P):
+    """A causal sliding window: tiles outside the band are skipped in both
+    simulators; turn orders and makespans agree."""
+    for c, r in ((3.0, 1.0), (1.0, 2.5)):
+        s = G.build(sched, B, Hq, Hkv, n, True, P, band=band)
+        want = G.simulate(s, c, r)
+        mk, turns, ntasks = dash.sim_schedule(sched, True, B, Hq, Hkv, n, P, c, r, band=band)
+        assert ntasks == len(s.tasks)
+        assert mk == pytest.approx(want.makespan)
+        if s.turn is not None:
+            np.testing.assert_array_equal(turns, oracle_turns(s, B, Hq, n))
+        # every dQ tile receives exactly the KV tiles of its band
+        for t in range(B * Hq * n):
+            i = t % n
+            got = sorted(j for j in turns[t] if j >= 0)
+            assert got == list(range(max(0, i - band + 1), i + 1))

@@ -51,10 +51,17 @@ inline int select_schedule(int D, int causal) {
 
 struct Shape {
     int B, Hq, Hkv, n, G, causal, sched;
+    int win;   // causal sliding window: tile diagonals 0 <= q - kv < win visited; 0 = none
 };
 
-// Symmetric shift only exists on causal masks; on a full mask it is shift.
-DASH_HD bool is_symmetric(const Shape& s) { return s.sched == kSymmetric && s.causal; }
+// Tile diagonals touched by a causal sliding window of `window` tokens: tile
+// pair (q, kv) holds a visible element iff 0 <= q - kv < band_tiles(window)
+// (the smallest query-key distance on diagonal t >= 1 is 128 t - 127).
+inline int band_tiles(int window) { return (window + 126) / 128 + 1; }
+
+// Symmetric shift only exists on causal masks without a window; otherwise it
+// is shift (a band leaves no triangle to fold).
+DASH_HD bool is_symmetric(const Shape& s) { return s.sched == kSymmetric && s.causal && !s.win; }
 DASH_HD bool is_static(int sched) { return sched == kShift || sched == kSymmetric; }
 DASH_HD bool is_ordered(int sched) { return sched != kAtomic; }
 
@@ -65,7 +72,14 @@ DASH_HD int64_t num_tasks(const Shape& s) {
 }
 
 // Visits of one KV tile j for ONE query head (non-symmetric schedules).
-DASH_HD int kv_len(const Shape& s, int j) { return s.causal ? s.n - j : s.n; }
+DASH_HD int kv_len(const Shape& s, int j) {
+    if (!s.causal) return s.n;
+    return (s.win && s.win < s.n - j) ? s.win : s.n - j;
+}
+
+// First KV tile that adds into dQ tile q (the rank base of the schedules
+// whose accumulation order is ascending KV).
+DASH_HD int first_kv(const Shape& s, int q) { return (s.causal && s.win && q >= s.win) ? q - s.win + 1 : 0; }
 
 // Pairs in task k (all heads of the group).
 DASH_HD int task_len(const Shape& s, int64_t k) {
@@ -96,7 +110,7 @@ DASH_HD Visit task_visit(const Shape& s, int64_t k, int u) {
         v.hq = v.hkv * s.G + g;
         v.kv = j;
         switch (s.sched) {
-            case kDescending: v.q = n - 1 - w; break;
+            case kDescending: v.q = (s.causal ? j : 0) + L - 1 - w; break;
             case kShift:
             case kSymmetric:  v.q = s.causal ? j + w : (j + w) % n; break;   // symmetric on a full mask = shift
             default:          v.q = (s.causal ? j : 0) + w; break;   // ascending, atomic

@@ -35,11 +35,11 @@ struct Model {
     std::vector<int64_t> entry;      // pair -> tile*n + kv
 };
 
-bool build(Model& m, int sched, int causal, int B, int Hq, int Hkv, int n, int P) {
+bool build(Model& m, int sched, int causal, int B, int Hq, int Hkv, int n, int P, int band = 0) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || n <= 0 || P <= 0 || Hq % Hkv || sched < 0 || sched > 4 ||
-        (causal != 0 && causal != 1))
+        (causal != 0 && causal != 1) || band < 0 || (band && !causal))
         return false;
-    m.s = Shape{B, Hq, Hkv, n, Hq / Hkv, causal, sched};
+    m.s = Shape{B, Hq, Hkv, n, Hq / Hkv, causal, sched, band};
     m.P = P;
     m.ntasks = dash::num_tasks(m.s);
     m.tiles = (int64_t)B * Hq * n;
@@ -167,11 +167,12 @@ bool dynamic_sim(const Model& m, const std::vector<std::vector<int64_t>>& order,
 
 }  // namespace
 
-extern "C" int dash_sim_schedule(int schedule, int causal, int B, int Hq, int Hkv, int n, int P, double c, double r,
-                                 double* makespan, int32_t* turn_order, int64_t* num_tasks) {
+namespace {
+int sim_impl(int schedule, int causal, int band, int B, int Hq, int Hkv, int n, int P, double c, double r,
+             double* makespan, int32_t* turn_order, int64_t* num_tasks) {
     Model m;
     try {
-        if (!build(m, schedule, causal, B, Hq, Hkv, n, P)) return DASH_ERR_ARG;
+        if (!build(m, schedule, causal, B, Hq, Hkv, n, P, band)) return DASH_ERR_ARG;
         auto order = accumulation_order(m);
         std::vector<double> end;
         bool ok;
@@ -201,6 +202,18 @@ extern "C" int dash_sim_schedule(int schedule, int causal, int B, int Hq, int Hk
         return DASH_ERR_NOMEM;
     }
     return DASH_OK;
+}
+}  // namespace
+
+extern "C" int dash_sim_schedule(int schedule, int causal, int B, int Hq, int Hkv, int n, int P, double c, double r,
+                                 double* makespan, int32_t* turn_order, int64_t* num_tasks) {
+    return sim_impl(schedule, causal, 0, B, Hq, Hkv, n, P, c, r, makespan, turn_order, num_tasks);
+}
+
+extern "C" int dash_sim_schedule_band(int schedule, int B, int Hq, int Hkv, int n, int band, int P, double c,
+                                      double r, double* makespan, int32_t* turn_order, int64_t* num_tasks) {
+    if (band < 1) return DASH_ERR_ARG;
+    return sim_impl(schedule, 1, band, B, Hq, Hkv, n, P, c, r, makespan, turn_order, num_tasks);
 }
 
 extern "C" int dash_sim_check_ranks(int schedule, int causal, int B, int Hq, int Hkv, int n, int P,

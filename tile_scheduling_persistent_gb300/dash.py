@@ -26,7 +26,7 @@ EXPORTS = (
     "dash_attn_bwd_preprocess", "dash_attn_bwd", "dash_dq_finalize", "dash_get_status", "dash_set_timeout_ns",
     "dash_release_workspaces", "dash_num_ctas", "dash_sim_schedule", "dash_sim_check_ranks",
     "dash_attn_bwd_debug", "dash_debug_tile_probe", "dash_attn_bwd_noalloc", "dash_select_schedule",
-    "dash_attn_fwd",
+    "dash_attn_fwd", "dash_sim_schedule_band",
 )
 
 
@@ -66,6 +66,7 @@ def lib():
     L.dash_release_workspaces.argtypes = []
     L.dash_num_ctas.argtypes = [I, ctypes.POINTER(I)]
     L.dash_sim_schedule.argtypes = [I] * 7 + [D, D, ctypes.POINTER(D), P, ctypes.POINTER(ctypes.c_int64)]
+    L.dash_sim_schedule_band.argtypes = [I] * 7 + [D, D, ctypes.POINTER(D), P, ctypes.POINTER(ctypes.c_int64)]
     L.dash_sim_check_ranks.argtypes = [I] * 7 + [P]
     L.dash_debug_tile_probe.argtypes = [P] * 6 + [I, I] + [P] * 7
     for name in EXPORTS:
@@ -195,14 +196,20 @@ def num_ctas(device=None):
     return P.value
 
 
-def sim_schedule(schedule, causal, B, Hq, Hkv, n, P, c=1.0, r=1.0, turn_order=True):
-    """Host DAG simulator: (makespan, turn order [B*Hq*n, n] or None, tasks)."""
+def sim_schedule(schedule, causal, B, Hq, Hkv, n, P, c=1.0, r=1.0, turn_order=True, band=None):
+    """Host DAG simulator: (makespan, turn order [B*Hq*n, n] or None, tasks).
+    band: tile diagonals of a causal sliding window (None: no window)."""
     mk = ctypes.c_double(0.0)
     nt = ctypes.c_int64(0)
     out = np.empty((B * Hq * n, n), dtype=np.int32) if turn_order else None
-    rc = lib().dash_sim_schedule(_sched(schedule), int(bool(causal)), B, Hq, Hkv, n, P, float(c), float(r),
-                                 ctypes.byref(mk), out.ctypes.data_as(ctypes.c_void_p) if out is not None else None,
-                                 ctypes.byref(nt))
+    optr = out.ctypes.data_as(ctypes.c_void_p) if out is not None else None
+    if band is None:
+        rc = lib().dash_sim_schedule(_sched(schedule), int(bool(causal)), B, Hq, Hkv, n, P, float(c), float(r),
+                                     ctypes.byref(mk), optr, ctypes.byref(nt))
+    else:
+        assert causal, "a band needs a causal mask"
+        rc = lib().dash_sim_schedule_band(_sched(schedule), B, Hq, Hkv, n, int(band), P, float(c), float(r),
+                                          ctypes.byref(mk), optr, ctypes.byref(nt))
     _check(rc, "dash_sim_schedule")
     return mk.value, out, nt.value
 
