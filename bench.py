@@ -58,8 +58,11 @@ def parse():
     return ap.parse_args()
 
 
-def flops_nominal(B, Hq, S, D, causal):
-    """Nominal backward FLOPs: 10*S^2*D per query head, halved for causal."""
+def flops_nominal(B, Hq, S, D, causal, window=None):
+    """Nominal backward FLOPs: 10*D per visible (query, key) pair per query
+    head: S^2 (full), S^2/2 (causal), S*W - W^2/2 (sliding window W < S)."""
+    if window is not None and window < S:
+        return 10.0 * D * B * Hq * (S * window - window * window / 2.0)
     f = 10.0 * S * S * D * B * Hq
     return f / 2 if causal else f
 
@@ -143,7 +146,7 @@ def gpu_inputs(w, seed, device):
     q, k, v, do = (t.to(device) for t in make_qkvdo(w.B, w.Hq, w.Hkv, w.S, w.D, seed, w.sigma_qkv, w.sigma_do))
     o = torch.empty_like(q)
     lse = torch.empty(w.B, w.Hq, w.S, dtype=torch.float32, device=device)
-    dash.attn_fwd(q, k, v, o, lse, w.causal)
+    dash.attn_fwd(q, k, v, o, lse, w.causal, window=w.window)
     code, info = dash.get_status()
     if code != 0:
         raise RuntimeError("forward: device status %d %s" % (code, info))
@@ -158,12 +161,12 @@ def time_forward(w, tensors, steps, warmup, stream):
     o = torch.empty_like(q)
     lse = torch.empty(w.B, w.Hq, w.S, dtype=torch.float32, device=q.device)
     for _ in range(warmup):
-        dash.attn_fwd(q, k, v, o, lse, w.causal, stream=stream)
+        dash.attn_fwd(q, k, v, o, lse, w.causal, stream=stream, window=w.window)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     a.record(stream)
     for _ in range(steps):
-        dash.attn_fwd(q, k, v, o, lse, w.causal, stream=stream)
+        dash.attn_fwd(q, k, v, o, lse, w.causal, stream=stream, window=w.window)
     b.record(stream)
     torch.cuda.synchronize()
     code, info = dash.get_status(stream)
@@ -185,11 +188,11 @@ def time_schedule(w, sched, tensors, outs, steps, warmup, stream, kernel_events=
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)   # torch creates events lazily: make both handles exist;
             e1.record(stream)   # the library re-records them around the kernel launch
-            dash.attn_bwd_debug(q, k, v, o, do, lse, dq, dk, dv, w.causal, sched, stream=stream,
+            dash.attn_bwd_debug(q, k, v, o, do, lse, dq, dk, dv, w.causal, sched, stream=stream, window=w.window,
                                 kernel_events=(e0, e1))
             evs.append((e0, e1))
         else:
-            dash.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, w.causal, sched, stream=stream)
+            dash.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, w.causal, sched, stream=stream, window=w.window)
         dash.dq_finalize(dq, dqb, stream=stream)
 
     for i in range(warmup):
@@ -234,7 +237,7 @@ def main_gpu(args):
     dv = torch.empty_like(dk)
     outs = (dq, dqb, dk, dv)
     stream = torch.cuda.current_stream()
-    flop = flops_nominal(w.B, w.Hq, w.S, w.D, w.causal)
+    flop = flops_nominal(w.B, w.Hq, w.S, w.D, w.causal, w.window)
     det = [s for s in w.schedules if s != "atomic_nondet"]
     if args.schedule:
         det = [args.schedule]
@@ -359,9 +362,10 @@ def wait_profile(w, sched, tensors, outs, warmup, stream, trace_out=None):
     P = dash.num_ctas()
     cyc = torch.zeros(P, 64, dtype=torch.int64, device=q.device)
     for _ in range(warmup):
-        dash.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, w.causal, sched, stream=stream)
+        dash.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, w.causal, sched, stream=stream, window=w.window)
     trace = torch.zeros(64, 32, dtype=torch.int64, device=q.device) if trace_out else None
     dash.attn_bwd_debug(q, k, v, o, do, lse, dq, dk, dv, w.causal, sched, stream=stream, wait_cycles=cyc,
+                        window=w.window,
                         event_trace=trace)
     torch.cuda.synchronize()
     if trace_out:
@@ -415,7 +419,7 @@ def e2e_run(w, sched, tensors, steps, warmup, stream):
         if used[i % 2]:
             stream.wait_event(ev["d2h"])         # step i-2's outputs have left the device
         q, k, v, o, do, lse = dev
-        dash.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, w.causal, sched, stream=stream)
+        dash.attn_bwd(q, k, v, o, do, lse, dq, dk, dv, w.causal, sched, stream=stream, window=w.window)
         dash.dq_finalize(dq, dqb, stream=stream)
         ev["comp"].record(stream)
         with torch.cuda.stream(s_out):
@@ -458,11 +462,11 @@ def oracle_sample_step(w, heads, seed=0):
     G = w.Hq // w.Hkv
     groups = max(1, heads // G)
     q, k, v, do = make_qkvdo(1, groups * G, groups, w.S, w.D, seed, w.sigma_qkv, w.sigma_do)
-    o, lse = A.attn_fwd(q, k, v, w.causal, row_block=2048, workers=_cpu_threads())
+    o, lse = A.attn_fwd(q, k, v, w.causal, row_block=2048, workers=_cpu_threads(), window=w.window)
     t0 = time.perf_counter()
-    A.attn_bwd(q, k, v, o, do, lse, w.causal, row_block=2048, workers=_cpu_threads())
+    A.attn_bwd(q, k, v, o, do, lse, w.causal, row_block=2048, workers=_cpu_threads(), window=w.window)
     dt = time.perf_counter() - t0
-    return dt, flops_nominal(1, groups * G, w.S, w.D, w.causal)
+    return dt, flops_nominal(1, groups * G, w.S, w.D, w.causal, w.window)
 
 
 def cpu_baseline(w, budget_s):

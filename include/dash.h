@@ -87,6 +87,27 @@ int dash_attn_fwd(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, da
                   int B, int Hq, int Hkv, int S, int D, int causal, dash_stream_t stream);
 
 /*
+ * dash_attn_bwd_window, dash_attn_fwd_window -- dash_attn_bwd and
+ * dash_attn_fwd for a causal sliding window of `window` tokens (>= 1): key
+ * j is visible to query i iff i - window < j <= i.  This is the band mask of
+ * the Ascend FlashAttentionGrad plan (ocdem.com, section 2.3.5, with tiles
+ * that are entirely masked skipped, section 3.1): a KV tile is visited only
+ * by the Q tiles of its band (band = ceil((window + 127) / 128) tile
+ * diagonals), the two edge diagonals are masked element by element, and
+ * the schedules, accumulation orders and rank tables are those of the band
+ * (symmetric shift runs as shift).  window >= S is the causal mask.  Same
+ * arguments (with `window` in place of `causal`), layouts, determinism and
+ * errors as the calls without a window; DASH_ERR_ARG also for window < 1.
+ */
+int dash_attn_bwd_window(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v,
+                         const dash_bf16* o, const dash_bf16* dO, const float* lse,
+                         float* dq, dash_bf16* dk, dash_bf16* dv,
+                         int B, int Hq, int Hkv, int S, int D, int window, int schedule,
+                         dash_stream_t stream);
+int dash_attn_fwd_window(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, dash_bf16* o, float* lse,
+                         int B, int Hq, int Hkv, int S, int D, int window, dash_stream_t stream);
+
+/*
  * dash_select_schedule -- the deterministic schedule that DASH_SCHED_AUTO
  * runs for this shape.  The DASH pages make the choice of strategy a matter
  * of the hardware: on H800 symmetric shift falls behind descending Q-tile
@@ -298,6 +319,9 @@ typedef struct {
      * events (MMA issues, softmax/drain/reduce milestones) for the first 64
      * pairs of CTA 0; event ids are listed in the kernel source. */
     unsigned long long* event_trace;
+    /* causal sliding window in tokens (as dash_attn_bwd_window), 0 = none;
+     * needs causal = 1 and no ranks_host. */
+    int window;
 } dash_debug_opts;
 
 /* dash_attn_bwd with debug hooks; same arguments and errors, plus

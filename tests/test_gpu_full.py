@@ -17,6 +17,7 @@ import pytest
 import torch
 
 from oracle import attention as A
+from oracle.dagsim import band_tiles
 from tile_scheduling_persistent_gb300 import dash
 from tile_scheduling_persistent_gb300.inputs import WORKLOADS, make_workload_inputs
 
@@ -55,14 +56,19 @@ def setup(name):
     q, k, v, do = make_workload_inputs(w, seed=0)
     dev = torch.device("cuda")
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
-    o, lse = gpu_forward_fp32(qd, kd, vd, w.causal)
+    if w.window:   # this library's forward (covered by its own parity tests) for the band
+        o = torch.empty_like(qd)
+        lse = torch.empty(w.B, w.Hq, w.S, dtype=torch.float32, device=dev)
+        dash.attn_fwd(qd, kd, vd, o, lse, True, window=w.window)
+    else:
+        o, lse = gpu_forward_fp32(qd, kd, vd, w.causal)
     G = w.Hq // w.Hkv
     exact = {}
     workers = min(8, len(os.sched_getaffinity(0)))
     for (b, hk) in sampled_groups(w):
         heads = list(range(hk * G, (hk + 1) * G))
         qs, ks, vs = q[b:b + 1, heads], k[b:b + 1, hk:hk + 1], v[b:b + 1, hk:hk + 1]
-        o_ex, lse_ex = A.attn_fwd(qs, ks, vs, w.causal, row_block=2048, workers=workers)
+        o_ex, lse_ex = A.attn_fwd(qs, ks, vs, w.causal, row_block=2048, workers=workers, window=w.window)
         exact[(b, hk)] = (o_ex, lse_ex)
         o[b, heads] = torch.from_numpy(o_ex[0]).to(torch.bfloat16).to(dev)
         lse[b, heads] = torch.from_numpy(lse_ex[0]).to(torch.float32).to(dev)
@@ -71,14 +77,14 @@ def setup(name):
     return _cache[name]
 
 
-def run_full(c, sched, **dbg):
+def run_full(c, sched, window=None, **dbg):
     dq = torch.empty(c.B, c.Hq, c.S, c.D, dtype=torch.float32, device="cuda")
     dk = torch.empty(c.B, c.Hkv, c.S, c.D, dtype=torch.bfloat16, device="cuda")
     dv = torch.empty_like(dk)
     if dbg:
-        dash.attn_bwd_debug(c.q, c.k, c.v, c.o, c.do, c.lse, dq, dk, dv, c.causal, sched, **dbg)
+        dash.attn_bwd_debug(c.q, c.k, c.v, c.o, c.do, c.lse, dq, dk, dv, c.causal, sched, window=window, **dbg)
     else:
-        dash.attn_bwd(c.q, c.k, c.v, c.o, c.do, c.lse, dq, dk, dv, c.causal, sched)
+        dash.attn_bwd(c.q, c.k, c.v, c.o, c.do, c.lse, dq, dk, dv, c.causal, sched, window=window)
     dqb = torch.empty(dq.shape, dtype=torch.bfloat16, device="cuda")
     dash.dq_finalize(dq, dqb)
     code, info = dash.get_status()
@@ -91,17 +97,22 @@ def test_full_size(name):
     w, c, host, exact = setup(name)
     q, k, v, do = host
     G = w.Hq // w.Hkv
-    nd = run_full(c, "atomic_nondet")
+    nd = run_full(c, "atomic_nondet", w.window)
     for sched in w.schedules:
         if sched == "atomic_nondet":
             got = nd
         else:
             log = torch.full((c.B * c.Hq * c.n, c.n), -1, dtype=torch.int32, device="cuda")
-            got = run_full(c, sched, order_log=log)
-            again = run_full(c, sched)
+            got = run_full(c, sched, w.window, order_log=log)
+            again = run_full(c, sched, w.window)
             for a, b in zip(got, again):
                 assert same_bits(a, b), sched
-            np.testing.assert_array_equal(log.cpu().numpy(), sim_turns(c, sched))
+            if w.window:
+                _, turns, _ = dash.sim_schedule(sched, True, c.B, c.Hq, c.Hkv, c.n, dash.num_ctas(),
+                                                band=band_tiles(w.window))
+            else:
+                turns = sim_turns(c, sched)
+            np.testing.assert_array_equal(log.cpu().numpy(), turns)
         dq, dqb, dk, dv = got
         for t in got:
             assert torch.isfinite(t.float()).all()
@@ -117,14 +128,14 @@ def test_full_size(name):
             rows, nr = rnd + edge, len(rnd)
             got_q, ref_q = [], []
             for gi, hq in enumerate(heads):
-                ref = A.dq_rows(qs, ks, vs, o_ex, dos, lse_ex, w.causal, 0, gi, rows)
+                ref = A.dq_rows(qs, ks, vs, o_ex, dos, lse_ex, w.causal, 0, gi, rows, window=w.window)
                 g = dqb[b, hq, rows].float().cpu().numpy().astype(np.float64)
                 assert np.abs(g - ref).max() <= MAX_ABS, (sched, "dq max-abs", b, hq)
                 got_q.append(g[:nr])
                 ref_q.append(ref[:nr])
             rel, _ = err(np.concatenate(got_q), np.concatenate(ref_q))
             assert rel <= REL_L2, (sched, "dq", b, hk, rel)
-            rk, rv = A.dkv_rows(qs, ks, vs, o_ex, dos, lse_ex, w.causal, 0, 0, rows)
+            rk, rv = A.dkv_rows(qs, ks, vs, o_ex, dos, lse_ex, w.causal, 0, 0, rows, window=w.window)
             for nm, g, ref in (("dk", dk[b, hk, rows], rk), ("dv", dv[b, hk, rows], rv)):
                 g = g.float().cpu().numpy().astype(np.float64)
                 assert np.abs(g - ref).max() <= MAX_ABS, (sched, nm + " max-abs", b, hk)

@@ -62,8 +62,9 @@ def test_cpp_matches_oracle_at_workload_shapes(name, P):
     for sched in w.schedules:
         if sched == "atomic_nondet":
             continue
-        s = G.build(sched, w.B, w.Hq, w.Hkv, n, w.causal, P)
-        _, turns, ntasks = dash.sim_schedule(sched, w.causal, w.B, w.Hq, w.Hkv, n, P, 1.0, 1.0)
+        band = G.band_tiles(w.window) if w.window else None
+        s = G.build(sched, w.B, w.Hq, w.Hkv, n, w.causal, P, band=band)
+        _, turns, ntasks = dash.sim_schedule(sched, w.causal, w.B, w.Hq, w.Hkv, n, P, 1.0, 1.0, band=band)
         assert ntasks == len(s.tasks)
         np.testing.assert_array_equal(turns, oracle_turns(s, w.B, w.Hq, n))
 

@@ -128,12 +128,16 @@ int validate_shape(int B, int Hq, int Hkv, int S, int D, int causal, int schedul
 
 int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const dash_bf16* o, const dash_bf16* dO,
              const float* lse, float* dq, dash_bf16* dk, dash_bf16* dv, int B, int Hq, int Hkv, int S, int D,
-             int causal, int schedule, cudaStream_t stream, const dash_debug_opts* dbg) {
+             int causal, int schedule, cudaStream_t stream, const dash_debug_opts* dbg, int window = 0) {
     const void* ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv};
     for (const void* ptr : ptrs)
         if (!aligned16(ptr)) return DASH_ERR_ARG;
     int rc = validate_shape(B, Hq, Hkv, S, D, causal, schedule);
     if (rc) return rc;
+    if (window < 0 || (window > 0 && !causal)) return DASH_ERR_ARG;
+    if (window >= S) window = 0;   // a window that covers the sequence is the causal mask
+    const int win = window ? band_tiles(window) : 0;
+    if (win && dbg && dbg->ranks_host) return DASH_ERR_ARG;   // the table check knows no window
     if (schedule == kAuto) schedule = select_schedule(D, causal);
     int dev = 0;
     if ((rc = check_device(&dev))) return rc;
@@ -143,7 +147,7 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
     if (rc) return DASH_ERR_CUDA;
 
     const int n = (S + 127) / 128;   // the last tile may be partial
-    const Shape sh{B, Hq, Hkv, n, Hq / Hkv, causal, schedule};
+    const Shape sh{B, Hq, Hkv, n, Hq / Hkv, causal, schedule, win};
     const long long tiles = (long long)B * Hq * n;
     const long long entries = tiles * n;
     const long long ntasks = num_tasks(sh);
@@ -166,14 +170,14 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
             return DASH_ERR_CUDA;
         ranks = (const uint16_t*)ws->dbg_ranks.p;
     } else if (is_static(schedule)) {
-        const long long key[8] = {B, Hq, Hkv, n, causal, is_symmetric(sh) ? kSymmetric : kShift, P, 0};
+        const long long key[8] = {B, Hq, Hkv, n, causal, is_symmetric(sh) ? kSymmetric : kShift, P, win};
         if (memcmp(key, ws->table_key, sizeof(key)) != 0) {
             if (ws->ranks.ensure((size_t)entries * sizeof(uint16_t)) ||
                 ws->time.ensure((size_t)entries * sizeof(uint32_t)) ||
                 ws->task_start.ensure((size_t)ntasks * sizeof(uint32_t)))
                 return DASH_ERR_NOMEM;
             if (launch_build_ranks(B, Hq, Hkv, n, causal, schedule, P, (uint16_t*)ws->ranks.p,
-                                   (uint32_t*)ws->time.p, (uint32_t*)ws->task_start.p, stream))
+                                   (uint32_t*)ws->time.p, (uint32_t*)ws->task_start.p, stream, win))
                 return DASH_ERR_CUDA;
             memcpy(ws->table_key, key, sizeof(key));
         }
@@ -224,6 +228,8 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
     prm.P = P;
     prm.scale = 1.0f / sqrtf((float)D);
     prm.scale_log2e = prm.scale * kLog2e;
+    prm.window = window;
+    prm.win = win;
     if (dbg && dbg->kernel_event_begin &&
         cudaEventRecord((cudaEvent_t)dbg->kernel_event_begin, stream) != cudaSuccess)
         return DASH_ERR_CUDA;
@@ -307,25 +313,47 @@ int dash_attn_bwd_debug(const dash_bf16* q, const dash_bf16* k, const dash_bf16*
                         int Hq, int Hkv, int S, int D, int causal, int schedule, dash_stream_t stream,
                         const dash_debug_opts* opts) {
     return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, S, D, causal, schedule, (cudaStream_t)stream,
-                    opts);
+                    opts, opts ? opts->window : 0);
 }
 
-int dash_attn_fwd(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, dash_bf16* o, float* lse, int B,
-                  int Hq, int Hkv, int S, int D, int causal, dash_stream_t stream_) {
+static int fwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, dash_bf16* o, float* lse, int B,
+                    int Hq, int Hkv, int S, int D, int causal, int window, dash_stream_t stream_) {
     cudaStream_t stream = (cudaStream_t)stream_;
     const void* ptrs[] = {q, k, v, o, lse};
     for (const void* ptr : ptrs)
         if (!aligned16(ptr)) return DASH_ERR_ARG;
     int rc = validate_shape(B, Hq, Hkv, S, D, causal, 0);
     if (rc) return rc;
+    if (window < 0 || (window > 0 && !causal)) return DASH_ERR_ARG;
+    if (window >= S) window = 0;
     int dev = 0;
     if ((rc = check_device(&dev))) return rc;
     Workspace* ws = get_ws(dev, stream);
     if (ws->ints.ensure((size_t)kIntHeader * sizeof(int))) return DASH_ERR_NOMEM;
     if (cudaMemsetAsync(ws->ints.p, 0, 8 * sizeof(int), stream) != cudaSuccess) return DASH_ERR_CUDA;
-    rc = launch_fwd(q, k, v, o, lse, (int*)ws->ints.p, B, Hq, Hkv, S, D, causal, g_timeout_ns.load(), stream);
+    rc = launch_fwd(q, k, v, o, lse, (int*)ws->ints.p, B, Hq, Hkv, S, D, causal, window, g_timeout_ns.load(),
+                    stream);
     if (rc == -1) return DASH_ERR_ARG;
     return rc ? DASH_ERR_CUDA : DASH_OK;
+}
+
+int dash_attn_fwd(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, dash_bf16* o, float* lse, int B,
+                  int Hq, int Hkv, int S, int D, int causal, dash_stream_t stream) {
+    return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, S, D, causal, 0, stream);
+}
+
+int dash_attn_fwd_window(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, dash_bf16* o, float* lse,
+                         int B, int Hq, int Hkv, int S, int D, int window, dash_stream_t stream) {
+    if (window < 1) return DASH_ERR_ARG;
+    return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, S, D, 1, window, stream);
+}
+
+int dash_attn_bwd_window(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const dash_bf16* o,
+                         const dash_bf16* dO, const float* lse, float* dq, dash_bf16* dk, dash_bf16* dv, int B,
+                         int Hq, int Hkv, int S, int D, int window, int schedule, dash_stream_t stream) {
+    if (window < 1) return DASH_ERR_ARG;
+    return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, S, D, 1, schedule, (cudaStream_t)stream, nullptr,
+                    window);
 }
 
 int dash_select_schedule(int B, int Hq, int Hkv, int S, int D, int causal) {

@@ -141,8 +141,8 @@ int launch_finalize(const float* src, void* dst, size_t numel, cudaStream_t s) {
 }
 
 int launch_build_ranks(int B, int Hq, int Hkv, int n, int causal, int sched, int P, uint16_t* ranks,
-                       uint32_t* time, uint32_t* task_start, cudaStream_t st) {
-    const Shape s{B, Hq, Hkv, n, Hq / Hkv, causal, sched};
+                       uint32_t* time, uint32_t* task_start, cudaStream_t st, int win) {
+    const Shape s{B, Hq, Hkv, n, Hq / Hkv, causal, sched, win};
     const long long ntasks = num_tasks(s);
     const long long entries = (long long)B * Hq * n * n;
     if (cudaMemsetAsync(time, 0xFF, (size_t)entries * sizeof(uint32_t), st) != cudaSuccess) return -2;

@@ -105,9 +105,10 @@ __device__ bool wait_turn(const BwdParams& p, const Ctl& c, volatile int* abort_
 
 }  // namespace
 
-// kTail: compiled for S % 128 != 0 (masks and guards of the partial last
-// tile); the instantiation for whole tiles carries none of that code.
-template <int D, bool kProf, bool kTail>
+// kMasked: compiled for a partial last tile (S % 128 != 0) or a sliding
+// window (their masks and guards); the instantiation for whole tiles and
+// plain masks carries none of that code.
+template <int D, bool kProf, bool kMasked>
 __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_constant__ BwdParams p) {
     using C = Cfg<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -167,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int slot = p.cta_perm ? p.cta_perm[blockIdx.x] : (int)blockIdx.x;
-    const Shape sh{p.B, p.Hq, p.Hkv, p.n, p.G, p.causal, p.sched};
+    const Shape sh{p.B, p.Hq, p.Hkv, p.n, p.G, p.causal, p.sched, p.win};
     const bool ordered = is_ordered(p.sched);
 
     // Each warpgroup first re-sizes its registers (all four warps execute the
@@ -214,7 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                     const bool last = (u == L - 1) || task_visit(sh, k, u + 1).kv != v.kv;
                     int rank = -1;
                     if (ordered)
-                        rank = p.ranks ? (int)p.ranks[rank_index(sh, v.b, v.hq, v.q, v.kv)] : v.kv;
+                        rank = p.ranks ? (int)p.ranks[rank_index(sh, v.b, v.hq, v.q, v.kv)] : v.kv - first_kv(sh, v.q);
                     d.b = v.b;
                     d.hq = v.hq;
                     d.hkv = v.hkv;
@@ -222,7 +223,9 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                     d.kv = v.kv;
                     d.flags = (first ? kKvFirst : 0) | (last ? kKvLast : 0) |
                               ((p.causal && v.q == v.kv) ? kDiag : 0) |
-                              ((kTail && (v.q == p.n - 1 || v.kv == p.n - 1)) ? kPartial : 0);
+                              ((kMasked && (((p.S & 127) && (v.q == p.n - 1 || v.kv == p.n - 1)) ||
+                                            (p.window && 128 * (v.q - v.kv) + 127 >= p.window)))
+                                   ? kPartial : 0);   // partial last tile, or the far edge of the window
                     d.rank = rank;
                     d.pad = 0;
                     descs[ds] = d;
@@ -411,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
             // (columns past S of a partial last tile read 0 and are masked)
             const int qcol = d.q * 128 + c0 + lane;
             const size_t qrow = (size_t)(d.b * p.Hq + d.hq) * p.S + (size_t)qcol;
-            const bool va = !kTail || qcol < p.S, vb = !kTail || qcol + 32 < p.S;
+            const bool va = !kMasked || qcol < p.S, vb = !kMasked || qcol + 32 < p.S;
             const float lse2_a = va ? ptx::ld_nc(p.lse + qrow) * kLog2e : 0.f;
             const float lse2_b = vb ? ptx::ld_nc(p.lse + qrow + 32) * kLog2e : 0.f;
             const float delta_a = va ? ptx::ld_nc(p.delta + qrow) : 0.f;
@@ -421,8 +424,9 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
             ptx::tc_fence_after();
             float P[64];
             unsigned long long tc0 = kProf ? clock64() : 0ull;
-            softmax_64<kTail || D == 64>(tmem + lane_off + C::COL_S, c0, lse2_a, lse2_b, p.scale_log2e, (d.flags & (kDiag | kPartial)) != 0,
-                       (d.flags & kDiag) != 0, row, p.S - d.kv * 128, p.S - d.q * 128, P);
+            softmax_64<kMasked || D == 64>(tmem + lane_off + C::COL_S, c0, lse2_a, lse2_b, p.scale_log2e, (d.flags & (kDiag | kPartial)) != 0,
+                       (d.flags & kDiag) != 0, row, p.S - d.kv * 128, p.S - d.q * 128,
+                       p.window ? p.window - 128 * (d.q - d.kv) : (1 << 30), P);
             prof_add(c, kRoleSoftmax, 8, tc0);
             ptx::tc_fence_before();
             __syncwarp();
@@ -542,8 +546,8 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
             if (!ok) break;
             if (rec) trace_ev<kProf>(p, pp, EV_DR_TURN);
             float* gdq = p.dq + ((size_t)(d.b * p.Hq + d.hq) * p.S + (size_t)d.q * 128) * D;
-            const bool row_a = !kTail || d.q * 128 + qa < p.S;   // rows past S
-            const bool row_b = !kTail || d.q * 128 + qa + 8 < p.S;
+            const bool row_a = !kMasked || d.q * 128 + qa < p.S;   // rows past S
+            const bool row_b = !kMasked || d.q * 128 + qa + 8 < p.S;
             const int cofs = 2 * (lane & 2);
 #pragma unroll
             for (int j = 0; j < D / 8; j += 2) {
@@ -569,7 +573,7 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                 if (!waitw(BAR(B_ACC_FULL), (uint32_t)(kvc & 1), c, kRoleDrain, (int)pp, 2)) break;
                 ptx::tc_fence_after();
                 const int krow = 32 * sub + lane;
-                const bool krow_ok = !kTail || d.kv * 128 + krow < p.S;   // rows past S are not stored
+                const bool krow_ok = !kMasked || d.kv * 128 + krow < p.S;   // rows past S are not stored
                 const size_t grow = ((size_t)(d.b * p.Hkv + d.hkv) * p.S + (size_t)d.kv * 128 + krow) * D;
                 __nv_bfloat16* out = (half == 0 ? p.dk : p.dv) + grow;
                 const uint32_t col = half == 0 ? C::COL_DK : C::COL_DV;
@@ -613,14 +617,14 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
     }
 }
 
-template <int D, bool kProf, bool kTail>
+template <int D, bool kProf, bool kMasked>
 int launch_bwd(const BwdParams& prm, int grid, cudaStream_t stream) {
     using C = Cfg<D>;
     static bool attr_done[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -2;
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(dash_bwd_kernel<D, kProf, kTail>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(dash_bwd_kernel<D, kProf, kMasked>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  C::kSmem) != cudaSuccess)
             return -2;
         attr_done[dev] = true;
@@ -630,12 +634,12 @@ int launch_bwd(const BwdParams& prm, int grid, cudaStream_t stream) {
     static int regs_ok[64] = {};
     if (dev >= 0 && dev < 64 && regs_ok[dev] == 0) {
         cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, dash_bwd_kernel<D, kProf, kTail>) != cudaSuccess) return -2;
+        if (cudaFuncGetAttributes(&fa, dash_bwd_kernel<D, kProf, kMasked>) != cudaSuccess) return -2;
         regs_ok[dev] = (fa.numRegs >= kRegsLaunch) ? 1 : -1;
     }
     if (dev < 0 || dev >= 64 || regs_ok[dev] != 1) return -3;
     void* args[] = {(void*)&prm};
-    cudaError_t e = cudaLaunchCooperativeKernel((const void*)dash_bwd_kernel<D, kProf, kTail>, dim3(grid),
+    cudaError_t e = cudaLaunchCooperativeKernel((const void*)dash_bwd_kernel<D, kProf, kMasked>, dim3(grid),
                                                 dim3(kThreads), args, C::kSmem, stream);
     if (e == cudaErrorCooperativeLaunchTooLarge) {
         (void)cudaGetLastError();
@@ -667,7 +671,7 @@ int bwd_max_ctas(int D, int device, int* P) {
 }
 
 int launch_bwd_dispatch(int D, const BwdParams& prm, int grid, cudaStream_t stream) {
-    if (prm.S % 128) {   // a partial last tile: the masked instantiation
+    if ((prm.S % 128) || prm.window) {   // a partial last tile or a window: the masked instantiation
         if (prm.prof)
             return D == 64 ? launch_bwd<64, true, true>(prm, grid, stream) : launch_bwd<128, true, true>(prm, grid, stream);
         return D == 64 ? launch_bwd<64, false, true>(prm, grid, stream) : launch_bwd<128, false, true>(prm, grid, stream);

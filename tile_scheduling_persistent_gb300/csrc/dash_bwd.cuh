@@ -173,6 +173,8 @@ struct BwdParams {
     long long ntasks;
     int B, Hq, Hkv, S, n, G, causal, sched, P;
     float scale, scale_log2e;
+    int window;                             // causal sliding window in tokens (0 = none)
+    int win;                                // its tile diagonals (band_tiles), 0 = none
 };
 
 // ------------------------------------------------------------------ MMA issue
@@ -237,15 +239,16 @@ __device__ __forceinline__ void issue_dq(uint32_t d_tmem, uint32_t sDsT, uint32_
 // 64-column span (so the MMA reads it as a K-major A operand).  lse2_* are
 // LSE * log2(e).  Works in 32-column halves to keep few registers live.
 // P is zero where row > column on a diagonal tile (`diag`) and, when `mask`
-// is set, where row >= lim_row (keys past S) or column >= lim_col (queries
-// past S).  kBranchMask: apply the masks in a branch taken only by masked
+// is set, where row >= lim_row (keys past S), column >= lim_col (queries
+// past S) or column - row >= wlim (query - key at or beyond a sliding
+// window: wlim = window - 128 * (q tile - kv tile)).  kBranchMask: apply the masks in a branch taken only by masked
 // pairs (needed for partial tiles; measured faster at D = 64); otherwise the
 // diagonal is applied with a per-element select (measured faster at D = 128
 // and then lim_row, lim_col must be >= 128).
 template <bool kBranchMask>
 __device__ __forceinline__ void softmax_64(uint32_t tmem_s_lane, int c0, float lse2_a, float lse2_b,
                                            float scale_log2e, bool mask, bool diag, int row, int lim_row,
-                                           int lim_col, float (&P)[64]) {
+                                           int lim_col, int wlim, float (&P)[64]) {
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
         uint32_t r[32];
@@ -262,7 +265,7 @@ __device__ __forceinline__ void softmax_64(uint32_t tmem_s_lane, int c0, float l
 #pragma unroll
             for (int k = 0; k < 32; ++k) {
                 const int col = c0 + 32 * h + k;
-                if ((diag && row > col) || row >= lim_row || col >= lim_col) P[32 * h + k] = 0.f;
+                if ((diag && row > col) || row >= lim_row || col >= lim_col || col - row >= wlim) P[32 * h + k] = 0.f;
             }
         }
         uint32_t pk[16];

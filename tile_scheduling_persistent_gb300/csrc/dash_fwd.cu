@@ -45,6 +45,8 @@ struct FwdParams {
     unsigned long long timeout_ns;
     int B, Hq, Hkv, S, n, G, causal;
     float scale_log2e;
+    int window;                     // causal sliding window in tokens (0 = none)
+    int win;                        // its tile diagonals (band_tiles), 0 = none
 };
 
 enum FwdBar : int {
@@ -119,9 +121,10 @@ __device__ bool fwaitw(uint32_t bar, uint32_t parity, const FwdWait& w, int role
     return ok != 0;
 }
 
-// kTail: compiled for S % 128 != 0 (masks and guards of the partial last
-// tile); the instantiation for whole tiles carries none of that code.
-template <int D, bool kTail>
+// kMasked: compiled for a partial last tile (S % 128 != 0) or a sliding
+// window (their masks and guards); the instantiation for whole tiles and
+// plain masks carries none of that code.
+template <int D, bool kMasked>
 __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant__ FwdParams p) {
     using C = FwdCfg<D>;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -141,7 +144,10 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
     const int qt = p.n - 1 - (int)(blockIdx.x % p.n);
     const int bh = (int)(blockIdx.x / p.n);
     const int b = bh / p.Hq, hq = bh % p.Hq, hkv = hq / p.G;
-    const int nkv = p.causal ? qt + 1 : p.n;
+    // KV tiles j0 .. j0 + nkv - 1 (a window starts the range at its far edge);
+    // loops count j from 0 and address the tile j0 + j
+    const int j0 = (p.causal && p.win && qt >= p.win) ? qt - p.win + 1 : 0;
+    const int nkv = p.causal ? qt - j0 + 1 : p.n;
     const int qrow = (b * p.Hq + hq) * p.S + qt * 128;   // first row of this tile in o / lse
     const int hqi = b * p.Hq + hq, hki = b * p.Hkv + hkv;  // head indices of the 3-D tensor maps
 
@@ -187,13 +193,13 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
                 ptx::mbar_arrive_expect_tx(BAR(F_K_FULL + st), C::kTile);
 #pragma unroll
                 for (int bx = 0; bx < C::kNBox; ++bx)
-                    ptx::tma_load_3d(sbase + C::OFF_K + st * C::kTile + bx * kBox, &p.tm_k, 64 * bx, j * 128, hki,
+                    ptx::tma_load_3d(sbase + C::OFF_K + st * C::kTile + bx * kBox, &p.tm_k, 64 * bx, (j0 + j) * 128, hki,
                                      BAR(F_K_FULL + st));
                 if (j >= 2 && !fwait1(BAR(F_V_EMPTY + st), (uint32_t)((j / 2 - 1) & 1), fw, 1, j)) break;
                 ptx::mbar_arrive_expect_tx(BAR(F_V_FULL + st), C::kTile);
 #pragma unroll
                 for (int bx = 0; bx < C::kNBox; ++bx)
-                    ptx::tma_load_3d(sbase + C::OFF_V + st * C::kTile + bx * kBox, &p.tm_v, 64 * bx, j * 128, hki,
+                    ptx::tma_load_3d(sbase + C::OFF_V + st * C::kTile + bx * kBox, &p.tm_v, 64 * bx, (j0 + j) * 128, hki,
                                      BAR(F_V_FULL + st));
                 issued = j + 1;
             }
@@ -270,13 +276,20 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
 #pragma unroll
                 for (int k = 0; k < 32; ++k) x[32 * h + k] = __uint_as_float(r[k]);   // raw scores
             }
-            if (p.causal && j == qt) {   // diagonal tile: key k visible to query row iff k <= row
+            const int jt = j0 + j;   // the KV tile
+            if (p.causal && jt == qt) {   // diagonal tile: key k visible to query row iff k <= row
 #pragma unroll
                 for (int k = 0; k < 128; ++k)
                     if (k > row) x[k] = -INFINITY;
             }
-            if (kTail && j == p.n - 1) {   // keys past S of the partial last tile
-                const int lim = p.S - j * 128;
+            if (kMasked && p.window && 128 * (qt - jt) + 127 >= p.window) {   // the window's far edge
+                const int wlim = p.window - 128 * (qt - jt);   // key k hidden from row iff row - k >= wlim
+#pragma unroll
+                for (int k = 0; k < 128; ++k)
+                    if (row - k >= wlim) x[k] = -INFINITY;
+            }
+            if (kMasked && jt == p.n - 1 && (p.S & 127)) {   // keys past S of the partial last tile
+                const int lim = p.S - jt * 128;
 #pragma unroll
                 for (int k = 0; k < 128; ++k)
                     if (k >= lim) x[k] = -INFINITY;
@@ -295,14 +308,17 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
             float alpha = 1.f;
             if (raise) {
                 const float m_new = fmaxf(m_ref, mx);
-                alpha = ptx::ex2(m_ref - m_new);   // 0 on the first tile (m_ref = -inf)
+                // 0 once the row has a first visible key (m_ref = -inf); a row
+                // with none yet (the window's far edge) stays at -inf, alpha 1
+                alpha = (m_new == -INFINITY) ? 1.f : ptx::ex2(m_ref - m_new);
                 m_ref = m_new;
             }
+            const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;   // P = 0, not NaN, for such a row
 #pragma unroll
             for (int i = 0; i < 8; ++i) part[i] = 0.f;
 #pragma unroll
             for (int k = 0; k < 128; ++k) {
-                x[k] = ptx::ex2(fmaf(x[k], c, -m_ref));
+                x[k] = ptx::ex2(fmaf(x[k], c, -m_use));
                 part[k & 7] += x[k];
             }
             const float rs = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
@@ -347,7 +363,7 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
             ok = fwaitw(BAR(F_O_DONE), (uint32_t)(jj & 1), fw, 3, nkv);
         if (ok) {
             ptx::tc_fence_after();
-            const bool row_ok = !kTail || qt * 128 + row < p.S;   // rows past S are not stored (loads stay warp-wide)
+            const bool row_ok = !kMasked || qt * 128 + row < p.S;   // rows past S are not stored (loads stay warp-wide)
             const float inv = 1.f / l;
             __nv_bfloat16* orow = p.o + ((size_t)qrow + row) * D;
 #pragma unroll
@@ -381,25 +397,25 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
     }
 }
 
-template <int D, bool kTail>
+template <int D, bool kMasked>
 int launch_fwd_t(const FwdParams& prm, int grid, cudaStream_t stream) {
     static bool attr_done[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -2;
     if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(dash_fwd_kernel<D, kTail>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(dash_fwd_kernel<D, kMasked>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  FwdCfg<D>::kSmem) != cudaSuccess)
             return -2;
         attr_done[dev] = true;
     }
-    dash_fwd_kernel<D, kTail><<<grid, 256, FwdCfg<D>::kSmem, stream>>>(prm);
+    dash_fwd_kernel<D, kMasked><<<grid, 256, FwdCfg<D>::kSmem, stream>>>(prm);
     return cudaGetLastError() == cudaSuccess ? 0 : -2;
 }
 
 }  // namespace
 
 int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int* status, int B, int Hq,
-               int Hkv, int S, int D, int causal, unsigned long long timeout_ns, cudaStream_t stream) {
+               int Hkv, int S, int D, int causal, int window, unsigned long long timeout_ns, cudaStream_t stream) {
     FwdParams prm;
     if (make_tmap_3d(&prm.tm_q, q, (long long)B * Hq, S, D) || make_tmap_3d(&prm.tm_k, k, (long long)B * Hkv, S, D) ||
         make_tmap_3d(&prm.tm_v, v, (long long)B * Hkv, S, D))
@@ -416,9 +432,11 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
     prm.G = Hq / Hkv;
     prm.causal = causal;
     prm.scale_log2e = (1.0f / sqrtf((float)D)) * kLog2e;
+    prm.window = window;
+    prm.win = window ? band_tiles(window) : 0;
     const long long grid = (long long)B * Hq * ((S + 127) / 128);
     if (grid <= 0 || grid > 0x7fffffffll) return -1;
-    if (S % 128)
+    if ((S % 128) || window)
         return D == 64 ? launch_fwd_t<64, true>(prm, (int)grid, stream) : launch_fwd_t<128, true>(prm, (int)grid, stream);
     return D == 64 ? launch_fwd_t<64, false>(prm, (int)grid, stream) : launch_fwd_t<128, false>(prm, (int)grid, stream);
 }

@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(256, 1) probe_kernel(const __grid_constant__ P
             for (int k = 0; k < 32; ++k) p.sT[row * 128 + c0 + 32 * h + k] = __uint_as_float(r[k]);
         }
         softmax_64<false>(tmem + lane_off + C::COL_S, c0, lse2_a, lse2_b, p.scale_log2e, p.diag != 0, p.diag != 0, row, 128,
-                   128, P);
+                   128, 1 << 30, P);
         for (int k = 0; k < 64; ++k) p.pT[row * 128 + c0 + k] = P[k];
         ptx::tc_fence_before();
     }

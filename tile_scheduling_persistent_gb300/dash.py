@@ -26,7 +26,7 @@ EXPORTS = (
     "dash_attn_bwd_preprocess", "dash_attn_bwd", "dash_dq_finalize", "dash_get_status", "dash_set_timeout_ns",
     "dash_release_workspaces", "dash_num_ctas", "dash_sim_schedule", "dash_sim_check_ranks",
     "dash_attn_bwd_debug", "dash_debug_tile_probe", "dash_attn_bwd_noalloc", "dash_select_schedule",
-    "dash_attn_fwd", "dash_sim_schedule_band",
+    "dash_attn_fwd", "dash_sim_schedule_band", "dash_attn_bwd_window", "dash_attn_fwd_window",
 )
 
 
@@ -41,7 +41,7 @@ class _DebugOpts(ctypes.Structure):
                 ("start_delay_ns", ctypes.c_void_p), ("ranks_host", ctypes.c_void_p),
                 ("skip_table_check", ctypes.c_int), ("kernel_event_begin", ctypes.c_void_p),
                 ("kernel_event_end", ctypes.c_void_p), ("wait_cycles", ctypes.c_void_p),
-                ("event_trace", ctypes.c_void_p)]
+                ("event_trace", ctypes.c_void_p), ("window", ctypes.c_int)]
 
 
 _lib = None
@@ -114,8 +114,15 @@ def _bwd_args(q, k, v, o, do, lse, dq, dk, dv, causal, schedule):
             _ptr(dk, bf), _ptr(dv, bf), B, Hq, Hkv, S, D, int(bool(causal)), _sched(schedule)]
 
 
-def attn_bwd(q, k, v, o, do, lse, dq, dk, dv, causal, schedule, stream=None):
-    """dq (fp32 accumulator, zeroed by the library), dk, dv (bf16) <- backward."""
+def attn_bwd(q, k, v, o, do, lse, dq, dk, dv, causal, schedule, stream=None, window=None):
+    """dq (fp32 accumulator, zeroed by the library), dk, dv (bf16) <- backward.
+    window: causal sliding window in tokens (needs causal=True), or None."""
+    if window is not None:
+        assert causal, "a sliding window needs a causal mask"
+        args = _bwd_args(q, k, v, o, do, lse, dq, dk, dv, causal, schedule)
+        args[-2] = int(window)   # the causal flag's slot carries the window
+        _check(lib().dash_attn_bwd_window(*args, _stream(stream)), "dash_attn_bwd_window")
+        return
     _check(lib().dash_attn_bwd(*_bwd_args(q, k, v, o, do, lse, dq, dk, dv, causal, schedule), _stream(stream)),
            "dash_attn_bwd")
 
@@ -129,8 +136,9 @@ def attn_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, causal, schedule, stream=N
 
 def attn_bwd_debug(q, k, v, o, do, lse, dq, dk, dv, causal, schedule, stream=None, order_log=None,
                    dq_partials=None, cta_perm=None, start_delay_ns=None, ranks_host=None, skip_table_check=False,
-                   kernel_events=None, wait_cycles=None, event_trace=None):
+                   kernel_events=None, wait_cycles=None, event_trace=None, window=None):
     opts = _DebugOpts()
+    opts.window = int(window) if window is not None else 0
     opts.wait_cycles = _ptr(wait_cycles, torch.int64)
     opts.event_trace = _ptr(event_trace, torch.int64)
     if kernel_events is not None:
@@ -173,13 +181,19 @@ def release_workspaces():
     _check(lib().dash_release_workspaces(), "dash_release_workspaces")
 
 
-def attn_fwd(q, k, v, o, lse, causal, stream=None):
-    """o (bf16 [B,Hq,S,D]) and lse (fp32 [B,Hq,S], natural log) <- forward."""
+def attn_fwd(q, k, v, o, lse, causal, stream=None, window=None):
+    """o (bf16 [B,Hq,S,D]) and lse (fp32 [B,Hq,S], natural log) <- forward.
+    window: causal sliding window in tokens (needs causal=True), or None."""
     B, Hq, S, D = q.shape
     Hkv = k.shape[1]
     bf = torch.bfloat16
-    _check(lib().dash_attn_fwd(_ptr(q, bf), _ptr(k, bf), _ptr(v, bf), _ptr(o, bf), _ptr(lse, torch.float32),
-                               B, Hq, Hkv, S, D, int(bool(causal)), _stream(stream)), "dash_attn_fwd")
+    ptrs = (_ptr(q, bf), _ptr(k, bf), _ptr(v, bf), _ptr(o, bf), _ptr(lse, torch.float32))
+    if window is not None:
+        assert causal, "a sliding window needs a causal mask"
+        _check(lib().dash_attn_fwd_window(*ptrs, B, Hq, Hkv, S, D, int(window), _stream(stream)),
+               "dash_attn_fwd_window")
+        return
+    _check(lib().dash_attn_fwd(*ptrs, B, Hq, Hkv, S, D, int(bool(causal)), _stream(stream)), "dash_attn_fwd")
 
 
 def select_schedule(B, Hq, Hkv, S, D, causal):

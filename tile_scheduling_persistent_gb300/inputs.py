@@ -37,6 +37,7 @@ class Workload:
     sigma_qkv: float
     sigma_do: float
     schedules: tuple
+    window: int | None = None   # causal sliding window in tokens (None: none)
 
 
 WORKLOADS = {
@@ -55,6 +56,11 @@ WORKLOADS = {
     "gqa_causal_b1_hq32_hkv8_s16384_d128": Workload(
         "gqa_causal_b1_hq32_hkv8_s16384_d128", True, 1, 32, 8, 16384, 128, 0.5, 1e-2,
         ("symmetric_shift", "descending_q", "shift", "serialized_ascending", "atomic_nondet")),
+    # a causal sliding window of 4096 tokens over 16K (the band mask of the
+    # Ascend plan; a Mistral-style long-context layer shape)
+    "window_b1_hq32_hkv8_s16384_d128_w4096": Workload(
+        "window_b1_hq32_hkv8_s16384_d128_w4096", True, 1, 32, 8, 16384, 128, 0.5, 1e-2,
+        ("shift", "descending_q", "serialized_ascending", "atomic_nondet"), window=4096),
 }
 
 
