@@ -274,6 +274,16 @@ int dash_sim_schedule_band(int schedule, int B, int Hq, int Hkv, int n, int band
                            int64_t* num_tasks);
 
 /*
+ * dash_sim_schedule_cross -- dash_sim_schedule for a full mask with nq query
+ * tiles and nkv key/value tiles per head (S_q != S_kv): each KV tile is one
+ * task that visits every query tile (shift rotates from tile kv mod nq).
+ * turn_order is int32 [B*Hq*nq][nkv].  Same outputs and errors otherwise.
+ */
+int dash_sim_schedule_cross(int schedule, int B, int Hq, int Hkv, int nq, int nkv, int P,
+                            double c, double r, double* makespan, int32_t* turn_order,
+                            int64_t* num_tasks);
+
+/*
  * dash_sim_check_ranks -- would the kernel complete with this accumulation
  * table?  ranks: host uint16 [B*Hq*n][n], rank of KV tile j's partial in dQ
  * tile i (entries of masked pairs are ignored).  The visit lists and SM

@@ -27,6 +27,11 @@ batch ``b`` and query head ``hq`` (key/value head ``hk = hq // (Hq // Hkv)``):
     dK_j  = sum over the heads hq of group hk, ascending, of scale * sum_i ds_ij q_i
     dV_j  = sum over the heads hq of group hk, ascending, of sum_i p_ij dO_i
 
+Query and key lengths may differ (``q`` [B,Hq,S_q,D], ``k``/``v`` [B,Hkv,S_kv,D]) for
+the full mask, as in the Ascend plan's tiling (ocdem.com, section 2.3.1:
+T_r = ceil(S1/128) query tiles, T_c = ceil(S2/128) key tiles); the causal
+mask and the window need S_q = S_kv.
+
 The sliding window (``window=W``, causal masks only) is the band mask of the
 Ascend plan (ocdem.com, section 2.3.5: lower-triangular and band masks, with
 tiles that are entirely masked skipped): key j is visible to query i iff
@@ -72,6 +77,11 @@ def _f64(x) -> np.ndarray:
 
 def _scale(D: int, scale: float | None) -> float:
     return 1.0 / math.sqrt(D) if scale is None else float(scale)
+
+
+def _check_lengths(q, k, causal: bool):
+    if causal and q.shape[2] != k.shape[2]:
+        raise ValueError("a causal mask needs equal query and key lengths")
 
 
 def _check_window(causal: bool, window):
@@ -121,6 +131,7 @@ def attn_fwd(q, k, v, causal: bool, scale: float | None = None,
     """Exact fp64 forward: returns (O [B,Hq,S,D], LSE [B,Hq,S])."""
     _check_window(causal, window)
     q, k, v = _f64(q), _f64(k), _f64(v)
+    _check_lengths(q, k, causal)
     B, Hq, S, D = q.shape
     Hkv = k.shape[1]
     G = Hq // Hkv
@@ -173,14 +184,16 @@ def attn_bwd(q, k, v, o, do, lse, causal: bool, scale: float | None = None,
     """
     _check_window(causal, window)
     q, k, v, o, do, lse = (_f64(x) for x in (q, k, v, o, do, lse))
+    _check_lengths(q, k, causal)
     B, Hq, S, D = q.shape
     Hkv = k.shape[1]
     G = Hq // Hkv
     sc = _scale(D, scale)
     delta = attn_bwd_delta(o, do)
     dq = np.empty_like(q)
-    part_k = np.empty_like(q)   # per-query-head contribution to dK / dV
-    part_v = np.empty_like(q)
+    Skv = k.shape[2]            # the key length may differ from the query length (full masks)
+    part_k = np.empty((B, Hq, Skv, D))   # per-query-head contribution to dK / dV
+    part_v = np.empty((B, Hq, Skv, D))
 
     def one(bh):
         b, hq = divmod(bh, Hq)

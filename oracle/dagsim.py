@@ -150,7 +150,7 @@ def symmetric_task(n: int, jp: int):
     return a, b
 
 
-def make_tasks(schedule: str, B: int, Hq: int, Hkv: int, n: int, causal: bool, band=None) -> list:
+def make_tasks(schedule: str, B: int, Hq: int, Hkv: int, n: int, causal: bool, band=None, nkv=None) -> list:
     """All tasks in dispatch order; each task is a list of Pair in run order."""
     if schedule not in SCHEDULES:
         raise ValueError(schedule)
@@ -166,18 +166,24 @@ def make_tasks(schedule: str, B: int, Hq: int, Hkv: int, n: int, causal: bool, b
                     t += [Pair(b, hq, i, kv) for hq in heads for (kv, i) in bb]
                     tasks.append(t)
             else:
-                for j in range(n):
+                for j in range(n if nkv is None else nkv):
                     tasks.append([Pair(b, hq, i, j) for hq in heads
                                   for i in visit_q(schedule, n, causal, j, band)])
     return tasks
 
 
-def build(schedule: str, B: int, Hq: int, Hkv: int, n: int, causal: bool, P: int, band=None) -> Schedule:
+def build(schedule: str, B: int, Hq: int, Hkv: int, n: int, causal: bool, P: int, band=None,
+          nkv=None) -> Schedule:
     """Tasks, assignment and accumulation order of a schedule (band: tile
-    diagonals of a sliding window, from band_tiles, or None)."""
+    diagonals of a sliding window, from band_tiles, or None; nkv: key/value
+    tiles per head when the key length differs from the query length, full
+    masks only -- one task per KV tile, visiting all n query tiles, shift
+    rotating from query tile kv mod n)."""
     if band is not None and (not causal or band < 1):
         raise ValueError("a band needs a causal mask and band >= 1")
-    tasks = make_tasks(schedule, B, Hq, Hkv, n, causal, band)
+    if nkv is not None and (causal or nkv < 1):
+        raise ValueError("S_q != S_kv needs a full mask")
+    tasks = make_tasks(schedule, B, Hq, Hkv, n, causal, band, nkv)
     static = schedule in STATIC
     s = Schedule(schedule, B, Hq, Hkv, n, causal, P, tasks, static)
     if static:

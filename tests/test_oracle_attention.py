@@ -332,3 +332,38 @@ def test_window_rejected_without_causal_mask():
 def test_window_flops():
     assert A.flops_nominal(1, 1, 1024, 64, True, window=256) == 10.0 * 64 * (1024 * 256 - 256 * 256 / 2)
     assert A.flops_nominal(1, 1, 1024, 64, True, window=4096) == A.flops_nominal(1, 1, 1024, 64, True)
+
+
+# ---- different query and key lengths (full mask) ----
+
+def test_cross_lengths_finite_differences_and_autograd():
+    B, Hq, Hkv, Sq, Skv, D = 1, 2, 1, 5, 9, 4
+    rng = np.random.default_rng(31)
+    q = rng.standard_normal((B, Hq, Sq, D))
+    k = rng.standard_normal((B, Hkv, Skv, D))
+    v = rng.standard_normal((B, Hkv, Skv, D))
+    do = rng.standard_normal((B, Hq, Sq, D))
+    o, lse = A.attn_fwd(q, k, v, False)
+    dq, dk, dv, _ = A.attn_bwd(q, k, v, o, do, lse, False)
+    assert dq.shape == q.shape and dk.shape == k.shape and dv.shape == v.shape
+    f = lambda: loss(q, k, v, do, False)  # noqa: E731
+    for x, g in ((q, dq), (k, dk), (v, dv)):
+        assert rel_err(g, fd_grad(f, x)) <= 1e-6
+    tq, tk, tv = (torch.tensor(x, dtype=torch.float64, requires_grad=True) for x in (q, k, v))
+    s = tq @ tk.repeat_interleave(2, dim=1).transpose(-1, -2) / 2.0
+    o_t = torch.softmax(s, dim=-1) @ tv.repeat_interleave(2, dim=1)
+    (o_t * torch.tensor(do)).sum().backward()
+    np.testing.assert_allclose(o, o_t.detach().numpy(), rtol=1e-12, atol=1e-12)
+    for a, b in ((dq, tq.grad), (dk, tk.grad), (dv, tv.grad)):
+        np.testing.assert_allclose(a, b.numpy(), rtol=1e-10, atol=1e-11)
+    r = [0, 4, 8]
+    dk_r, dv_r = A.dkv_rows(q, k, v, o, do, lse, False, 0, 0, r)
+    np.testing.assert_allclose(dk_r, dk[0, 0, r], atol=1e-13)
+    np.testing.assert_allclose(dv_r, dv[0, 0, r], atol=1e-13)
+    np.testing.assert_allclose(A.dq_rows(q, k, v, o, do, lse, False, 0, 1, [0, 3]), dq[0, 1, [0, 3]], atol=1e-13)
+
+
+def test_cross_lengths_need_a_full_mask():
+    q, k, v, _ = make(1, 1, 1, 4, 4, seed=32)
+    with pytest.raises(ValueError):
+        A.attn_fwd(q, np.concatenate([k, k], axis=2), np.concatenate([v, v], axis=2), True)

@@ -127,3 +127,29 @@ def test_cpp_matches_oracle_with_a_band(sched, B, Hq, Hkv, n, band, P):
             i = t % n
             got = sorted(j for j in turns[t] if j >= 0)
             assert got == list(range(max(0, i - band + 1), i + 1))
+
+
+CROSS_CASES = [(sched, B, Hq, Hkv, nq, nkv, P)
+               for sched in G.SCHEDULES
+               for (B, Hq, Hkv, nq, nkv, P) in [(1, 1, 1, 3, 7, 4), (1, 2, 2, 6, 2, 3), (2, 4, 2, 5, 9, 5),
+                                                (1, 2, 1, 1, 4, 16), (1, 3, 3, 8, 1, 2)]]
+
+
+@pytest.mark.parametrize("sched,B,Hq,Hkv,nq,nkv,P", CROSS_CASES)
+def test_cpp_matches_oracle_with_different_lengths(sched, B, Hq, Hkv, nq, nkv, P):
+    """Full mask, nq query tiles and nkv key/value tiles: both simulators give
+    the same makespans and turn orders, and every dQ tile receives every KV tile."""
+    for c, r in ((3.0, 1.0), (1.0, 2.5)):
+        s = G.build(sched, B, Hq, Hkv, nq, False, P, nkv=nkv)
+        want = G.simulate(s, c, r)
+        mk, turns, ntasks = dash.sim_schedule(sched, False, B, Hq, Hkv, nq, P, c, r, nkv=nkv)
+        assert turns.shape == (B * Hq * nq, nkv)
+        assert ntasks == len(s.tasks) == B * Hkv * nkv
+        assert mk == pytest.approx(want.makespan)
+        if s.turn is not None:
+            out = np.full((B * Hq * nq, nkv), -1, np.int32)
+            for (b, hq, i), js in s.turn.items():
+                out[(b * Hq + hq) * nq + i, :len(js)] = js
+            np.testing.assert_array_equal(turns, out)
+            for row in turns:
+                assert sorted(row) == list(range(nkv))

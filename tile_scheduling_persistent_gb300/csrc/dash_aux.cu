@@ -90,6 +90,7 @@ __global__ void pair_time_kernel(Shape s, long long ntasks, const uint32_t* task
 }
 
 __global__ void rank_kernel(int n, long long entries, const uint32_t* time, uint16_t* ranks) {
+    // n: key/value tiles per head (the row length of the tables)
     const long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (e >= entries) return;
     const long long tile = e / n;
@@ -141,14 +142,15 @@ int launch_finalize(const float* src, void* dst, size_t numel, cudaStream_t s) {
 }
 
 int launch_build_ranks(int B, int Hq, int Hkv, int n, int causal, int sched, int P, uint16_t* ranks,
-                       uint32_t* time, uint32_t* task_start, cudaStream_t st, int win) {
-    const Shape s{B, Hq, Hkv, n, Hq / Hkv, causal, sched, win};
+                       uint32_t* time, uint32_t* task_start, cudaStream_t st, int win, int nk) {
+    const Shape s{B, Hq, Hkv, n, Hq / Hkv, causal, sched, win, nk};
+    const int nkv = num_kv(s);
     const long long ntasks = num_tasks(s);
-    const long long entries = (long long)B * Hq * n * n;
+    const long long entries = (long long)B * Hq * n * nkv;
     if (cudaMemsetAsync(time, 0xFF, (size_t)entries * sizeof(uint32_t), st) != cudaSuccess) return -2;
     task_start_kernel<<<(P + 127) / 128, 128, 0, st>>>(s, P, ntasks, task_start);
     pair_time_kernel<<<(unsigned)((ntasks + 127) / 128), 128, 0, st>>>(s, ntasks, task_start, time);
-    rank_kernel<<<(unsigned)((entries + 255) / 256), 256, 0, st>>>(n, entries, time, ranks);
+    rank_kernel<<<(unsigned)((entries + 255) / 256), 256, 0, st>>>(nkv, entries, time, ranks);
     return cudaGetLastError() == cudaSuccess ? 0 : -2;
 }
 

@@ -19,7 +19,7 @@ int launch_finalize(const float* src, void* dst, size_t numel, cudaStream_t s);
 // ranks [B*Hq*n][n] (uint16), scratch `time` [B*Hq*n][n] (uint32),
 // `task_start` [num_tasks] (uint32).
 int launch_build_ranks(int B, int Hq, int Hkv, int n, int causal, int sched, int P, uint16_t* ranks,
-                       uint32_t* time, uint32_t* task_start, cudaStream_t s, int win = 0);
+                       uint32_t* time, uint32_t* task_start, cudaStream_t s, int win = 0, int nk = 0);
 
 // Attention forward (dash_fwd.cu): O bf16 [B,Hq,S,D], LSE fp32 [B,Hq,S];
 // status = the stream workspace's status word (cleared by the caller).

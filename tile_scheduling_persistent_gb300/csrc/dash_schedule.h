@@ -50,9 +50,13 @@ inline int select_schedule(int D, int causal) {
 }
 
 struct Shape {
-    int B, Hq, Hkv, n, G, causal, sched;
+    int B, Hq, Hkv, n, G, causal, sched;   // n: query tiles per head
     int win;   // causal sliding window: tile diagonals 0 <= q - kv < win visited; 0 = none
+    int nk;    // key/value tiles per head when they differ from n (full masks only); 0 = n
 };
+
+// Key/value tiles per head.
+DASH_HD int num_kv(const Shape& s) { return s.nk ? s.nk : s.n; }
 
 // Tile diagonals touched by a causal sliding window of `window` tokens: tile
 // pair (q, kv) holds a visible element iff 0 <= q - kv < band_tiles(window)
@@ -66,7 +70,7 @@ DASH_HD bool is_static(int sched) { return sched == kShift || sched == kSymmetri
 DASH_HD bool is_ordered(int sched) { return sched != kAtomic; }
 
 // Tasks per (b, hkv) and in total.
-DASH_HD int tasks_per_group(const Shape& s) { return is_symmetric(s) ? (s.n + 1) / 2 : s.n; }
+DASH_HD int tasks_per_group(const Shape& s) { return is_symmetric(s) ? (s.n + 1) / 2 : num_kv(s); }
 DASH_HD int64_t num_tasks(const Shape& s) {
     return (int64_t)s.B * s.Hkv * tasks_per_group(s);
 }
@@ -144,7 +148,7 @@ DASH_HD Visit task_visit(const Shape& s, int64_t k, int u) {
 
 // Index of the accumulation-rank entry of pair (b, hq, q, kv).
 DASH_HD int64_t rank_index(const Shape& s, int b, int hq, int q, int kv) {
-    return (((int64_t)b * s.Hq + hq) * s.n + q) * s.n + kv;
+    return (((int64_t)b * s.Hq + hq) * s.n + q) * num_kv(s) + kv;
 }
 
 }  // namespace dash

@@ -35,11 +35,12 @@ struct Model {
     std::vector<int64_t> entry;      // pair -> tile*n + kv
 };
 
-bool build(Model& m, int sched, int causal, int B, int Hq, int Hkv, int n, int P, int band = 0) {
+bool build(Model& m, int sched, int causal, int B, int Hq, int Hkv, int n, int P, int band = 0, int nk = 0) {
     if (B <= 0 || Hq <= 0 || Hkv <= 0 || n <= 0 || P <= 0 || Hq % Hkv || sched < 0 || sched > 4 ||
-        (causal != 0 && causal != 1) || band < 0 || (band && !causal))
+        (causal != 0 && causal != 1) || band < 0 || (band && !causal) || nk < 0 || (nk && causal))
         return false;
-    m.s = Shape{B, Hq, Hkv, n, Hq / Hkv, causal, sched, band};
+    m.s = Shape{B, Hq, Hkv, n, Hq / Hkv, causal, sched, band, nk == n ? 0 : nk};
+    const int nkv = dash::num_kv(m.s);
     m.P = P;
     m.ntasks = dash::num_tasks(m.s);
     m.tiles = (int64_t)B * Hq * n;
@@ -60,7 +61,7 @@ bool build(Model& m, int sched, int causal, int B, int Hq, int Hkv, int n, int P
             const int64_t p = m.task_off[k] + u;
             m.tile[p] = ((int64_t)v.b * Hq + v.hq) * n + v.q;
             m.kv[p] = v.kv;
-            m.entry[p] = m.tile[p] * n + v.kv;
+            m.entry[p] = m.tile[p] * nkv + v.kv;
         }
     }
     return true;
@@ -169,10 +170,11 @@ bool dynamic_sim(const Model& m, const std::vector<std::vector<int64_t>>& order,
 
 namespace {
 int sim_impl(int schedule, int causal, int band, int B, int Hq, int Hkv, int n, int P, double c, double r,
-             double* makespan, int32_t* turn_order, int64_t* num_tasks) {
+             double* makespan, int32_t* turn_order, int64_t* num_tasks, int nk = 0) {
     Model m;
     try {
-        if (!build(m, schedule, causal, B, Hq, Hkv, n, P, band)) return DASH_ERR_ARG;
+        if (!build(m, schedule, causal, B, Hq, Hkv, n, P, band, nk)) return DASH_ERR_ARG;
+        const int nkv = dash::num_kv(m.s);
         auto order = accumulation_order(m);
         std::vector<double> end;
         bool ok;
@@ -193,8 +195,8 @@ int sim_impl(int schedule, int causal, int band, int B, int Hq, int Hkv, int n, 
                     });
             }
             for (int64_t t = 0; t < m.tiles; ++t) {
-                int32_t* row = turn_order + t * n;
-                for (int i = 0; i < n; ++i) row[i] = -1;
+                int32_t* row = turn_order + t * nkv;
+                for (int i = 0; i < nkv; ++i) row[i] = -1;
                 for (size_t i = 0; i < order[t].size(); ++i) row[i] = m.kv[order[t][i]];
             }
         }
@@ -214,6 +216,12 @@ extern "C" int dash_sim_schedule_band(int schedule, int B, int Hq, int Hkv, int 
                                       double r, double* makespan, int32_t* turn_order, int64_t* num_tasks) {
     if (band < 1) return DASH_ERR_ARG;
     return sim_impl(schedule, 1, band, B, Hq, Hkv, n, P, c, r, makespan, turn_order, num_tasks);
+}
+
+extern "C" int dash_sim_schedule_cross(int schedule, int B, int Hq, int Hkv, int nq, int nkv, int P, double c,
+                                       double r, double* makespan, int32_t* turn_order, int64_t* num_tasks) {
+    if (nkv < 1) return DASH_ERR_ARG;
+    return sim_impl(schedule, 0, 0, B, Hq, Hkv, nq, P, c, r, makespan, turn_order, num_tasks, nkv);
 }
 
 extern "C" int dash_sim_check_ranks(int schedule, int causal, int B, int Hq, int Hkv, int n, int P,

@@ -27,6 +27,7 @@ EXPORTS = (
     "dash_release_workspaces", "dash_num_ctas", "dash_sim_schedule", "dash_sim_check_ranks",
     "dash_attn_bwd_debug", "dash_debug_tile_probe", "dash_attn_bwd_noalloc", "dash_select_schedule",
     "dash_attn_fwd", "dash_sim_schedule_band", "dash_attn_bwd_window", "dash_attn_fwd_window",
+    "dash_sim_schedule_cross",
 )
 
 
@@ -67,6 +68,7 @@ def lib():
     L.dash_num_ctas.argtypes = [I, ctypes.POINTER(I)]
     L.dash_sim_schedule.argtypes = [I] * 7 + [D, D, ctypes.POINTER(D), P, ctypes.POINTER(ctypes.c_int64)]
     L.dash_sim_schedule_band.argtypes = [I] * 7 + [D, D, ctypes.POINTER(D), P, ctypes.POINTER(ctypes.c_int64)]
+    L.dash_sim_schedule_cross.argtypes = [I] * 7 + [D, D, ctypes.POINTER(D), P, ctypes.POINTER(ctypes.c_int64)]
     L.dash_sim_check_ranks.argtypes = [I] * 7 + [P]
     L.dash_debug_tile_probe.argtypes = [P] * 6 + [I, I] + [P] * 7
     for name in EXPORTS:
@@ -210,14 +212,20 @@ def num_ctas(device=None):
     return P.value
 
 
-def sim_schedule(schedule, causal, B, Hq, Hkv, n, P, c=1.0, r=1.0, turn_order=True, band=None):
-    """Host DAG simulator: (makespan, turn order [B*Hq*n, n] or None, tasks).
-    band: tile diagonals of a causal sliding window (None: no window)."""
+def sim_schedule(schedule, causal, B, Hq, Hkv, n, P, c=1.0, r=1.0, turn_order=True, band=None, nkv=None):
+    """Host DAG simulator: (makespan, turn order [B*Hq*n, nkv] or None, tasks).
+    band: tile diagonals of a causal sliding window (None: no window);
+    nkv: key/value tiles per head when they differ from n (full masks only)."""
     mk = ctypes.c_double(0.0)
     nt = ctypes.c_int64(0)
-    out = np.empty((B * Hq * n, n), dtype=np.int32) if turn_order else None
+    nk = n if nkv is None else int(nkv)
+    out = np.empty((B * Hq * n, nk), dtype=np.int32) if turn_order else None
     optr = out.ctypes.data_as(ctypes.c_void_p) if out is not None else None
-    if band is None:
+    if nkv is not None:
+        assert not causal and band is None, "S_q != S_kv needs a full mask"
+        rc = lib().dash_sim_schedule_cross(_sched(schedule), B, Hq, Hkv, n, nk, P, float(c), float(r),
+                                           ctypes.byref(mk), optr, ctypes.byref(nt))
+    elif band is None:
         rc = lib().dash_sim_schedule(_sched(schedule), int(bool(causal)), B, Hq, Hkv, n, P, float(c), float(r),
                                      ctypes.byref(mk), optr, ctypes.byref(nt))
     else:
