@@ -58,9 +58,12 @@ def parse():
     return ap.parse_args()
 
 
-def flops_nominal(B, Hq, S, D, causal, window=None):
+def flops_nominal(B, Hq, S, D, causal, window=None, Skv=None):
     """Nominal backward FLOPs: 10*D per visible (query, key) pair per query
-    head: S^2 (full), S^2/2 (causal), S*W - W^2/2 (sliding window W < S)."""
+    head: S^2 (full), S*Skv (full, key length Skv), S^2/2 (causal),
+    S*W - W^2/2 (sliding window W < S)."""
+    if Skv is not None and Skv != S:
+        return 10.0 * D * B * Hq * S * Skv
     if window is not None and window < S:
         return 10.0 * D * B * Hq * (S * window - window * window / 2.0)
     f = 10.0 * S * S * D * B * Hq
@@ -143,7 +146,8 @@ def gpu_inputs(w, seed, device):
     import torch
     from tile_scheduling_persistent_gb300 import dash
     from tile_scheduling_persistent_gb300.inputs import make_qkvdo
-    q, k, v, do = (t.to(device) for t in make_qkvdo(w.B, w.Hq, w.Hkv, w.S, w.D, seed, w.sigma_qkv, w.sigma_do))
+    q, k, v, do = (t.to(device) for t in make_qkvdo(w.B, w.Hq, w.Hkv, w.S, w.D, seed, w.sigma_qkv, w.sigma_do,
+                                                                    w.Skv))
     o = torch.empty_like(q)
     lse = torch.empty(w.B, w.Hq, w.S, dtype=torch.float32, device=device)
     dash.attn_fwd(q, k, v, o, lse, w.causal, window=w.window)
@@ -233,11 +237,11 @@ def main_gpu(args):
     tensors = gpu_inputs(w, seed=rank, device=device)
     dq = torch.empty(w.B, w.Hq, w.S, w.D, dtype=torch.float32, device=device)
     dqb = torch.empty(dq.shape, dtype=torch.bfloat16, device=device)
-    dk = torch.empty(w.B, w.Hkv, w.S, w.D, dtype=torch.bfloat16, device=device)
+    dk = torch.empty(w.B, w.Hkv, w.Skv or w.S, w.D, dtype=torch.bfloat16, device=device)
     dv = torch.empty_like(dk)
     outs = (dq, dqb, dk, dv)
     stream = torch.cuda.current_stream()
-    flop = flops_nominal(w.B, w.Hq, w.S, w.D, w.causal, w.window)
+    flop = flops_nominal(w.B, w.Hq, w.S, w.D, w.causal, w.window, w.Skv)
     det = [s for s in w.schedules if s != "atomic_nondet"]
     if args.schedule:
         det = [args.schedule]
@@ -397,7 +401,7 @@ def e2e_run(w, sched, tensors, steps, warmup, stream):
         dev = [torch.empty_like(t) for t in tensors]
         dq = torch.empty(w.B, w.Hq, w.S, w.D, dtype=torch.float32, device=dev[0].device)
         dqb = torch.empty(dq.shape, dtype=torch.bfloat16, device=dq.device)
-        dk = torch.empty(w.B, w.Hkv, w.S, w.D, dtype=torch.bfloat16, device=dq.device)
+        dk = torch.empty(w.B, w.Hkv, w.Skv or w.S, w.D, dtype=torch.bfloat16, device=dq.device)
         dv = torch.empty_like(dk)
         out_host = [torch.empty(x.shape, dtype=x.dtype).pin_memory() for x in (dqb, dk, dv)]
         ev = {k: torch.cuda.Event() for k in ("h2d", "comp", "d2h")}
@@ -461,12 +465,12 @@ def oracle_sample_step(w, heads, seed=0):
     from tile_scheduling_persistent_gb300.inputs import make_qkvdo
     G = w.Hq // w.Hkv
     groups = max(1, heads // G)
-    q, k, v, do = make_qkvdo(1, groups * G, groups, w.S, w.D, seed, w.sigma_qkv, w.sigma_do)
+    q, k, v, do = make_qkvdo(1, groups * G, groups, w.S, w.D, seed, w.sigma_qkv, w.sigma_do, w.Skv)
     o, lse = A.attn_fwd(q, k, v, w.causal, row_block=2048, workers=_cpu_threads(), window=w.window)
     t0 = time.perf_counter()
     A.attn_bwd(q, k, v, o, do, lse, w.causal, row_block=2048, workers=_cpu_threads(), window=w.window)
     dt = time.perf_counter() - t0
-    return dt, flops_nominal(1, groups * G, w.S, w.D, w.causal, w.window)
+    return dt, flops_nominal(1, groups * G, w.S, w.D, w.causal, w.window, w.Skv)
 
 
 def cpu_baseline(w, budget_s):

@@ -108,6 +108,24 @@ int dash_attn_fwd_window(const dash_bf16* q, const dash_bf16* k, const dash_bf16
                          int B, int Hq, int Hkv, int S, int D, int window, dash_stream_t stream);
 
 /*
+ * dash_attn_bwd_cross, dash_attn_fwd_cross -- dash_attn_bwd and dash_attn_fwd
+ * with a key/value length Skv different from the query length Sq (full mask):
+ * q, o, dO, dq: [B,Hq,Sq,D]; lse: [B,Hq,Sq]; k, v, dk, dv: [B,Hkv,Skv,D].  The
+ * Ascend plan's tiling (ocdem.com, section 2.3.1): ceil(Sq/128) query tiles
+ * by ceil(Skv/128) key tiles; each KV tile is one task that visits every
+ * query tile (shift rotates from query tile kv mod nq; symmetric shift is
+ * shift).  Same arguments otherwise (no causal flag), same determinism and
+ * errors.
+ */
+int dash_attn_bwd_cross(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v,
+                        const dash_bf16* o, const dash_bf16* dO, const float* lse,
+                        float* dq, dash_bf16* dk, dash_bf16* dv,
+                        int B, int Hq, int Hkv, int Sq, int Skv, int D, int schedule,
+                        dash_stream_t stream);
+int dash_attn_fwd_cross(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, dash_bf16* o, float* lse,
+                        int B, int Hq, int Hkv, int Sq, int Skv, int D, dash_stream_t stream);
+
+/*
  * dash_select_schedule -- the deterministic schedule that DASH_SCHED_AUTO
  * runs for this shape.  The DASH pages make the choice of strategy a matter
  * of the hardware: on H800 symmetric shift falls behind descending Q-tile
@@ -299,11 +317,12 @@ int dash_sim_check_ranks(int schedule, int causal, int B, int Hq, int Hkv, int n
  * ------------------------------------------------------------------------- */
 
 typedef struct {
-    /* device int32 [B*Hq*n][n] or NULL: slot k of dQ tile t receives the KV
-     * index of the k-th partial actually added (log written as it happens). */
+    /* device int32 [B*Hq*n][nkv] or NULL (n, nkv: query and key/value tiles
+     * per head): slot k of dQ tile t receives the KV index of the k-th
+     * partial actually added (log written as it happens). */
     int32_t* order_log;
-    /* device fp32 [B*Hq*n*n][128][D] or NULL: the fp32 dQ partial of pair
-     * (b,hq,i,j) at index ((b*Hq+hq)*n+i)*n+j, as produced by the MMA. */
+    /* device fp32 [B*Hq*n*nkv][128][D] or NULL: the fp32 dQ partial of pair
+     * (b,hq,i,j) at index ((b*Hq+hq)*n+i)*nkv+j, as produced by the MMA. */
     float* dq_partials;
     /* device int32 [P] or NULL: worker slot used by CTA blockIdx.x (a
      * permutation of 0..P-1). */
@@ -332,6 +351,9 @@ typedef struct {
     /* causal sliding window in tokens (as dash_attn_bwd_window), 0 = none;
      * needs causal = 1 and no ranks_host. */
     int window;
+    /* key/value length when it differs from S (as dash_attn_bwd_cross),
+     * 0 = S; needs causal = 0 and no ranks_host. */
+    int skv;
 } dash_debug_opts;
 
 /* dash_attn_bwd with debug hooks; same arguments and errors, plus

@@ -56,10 +56,10 @@ def setup(name):
     q, k, v, do = make_workload_inputs(w, seed=0)
     dev = torch.device("cuda")
     qd, kd, vd, dod = (t.to(dev) for t in (q, k, v, do))
-    if w.window:   # this library's forward (covered by its own parity tests) for the band
+    if w.window or w.Skv:   # this library's forward (covered by its own parity tests)
         o = torch.empty_like(qd)
         lse = torch.empty(w.B, w.Hq, w.S, dtype=torch.float32, device=dev)
-        dash.attn_fwd(qd, kd, vd, o, lse, True, window=w.window)
+        dash.attn_fwd(qd, kd, vd, o, lse, w.causal, window=w.window)
     else:
         o, lse = gpu_forward_fp32(qd, kd, vd, w.causal)
     G = w.Hq // w.Hkv
@@ -79,7 +79,7 @@ def setup(name):
 
 def run_full(c, sched, window=None, **dbg):
     dq = torch.empty(c.B, c.Hq, c.S, c.D, dtype=torch.float32, device="cuda")
-    dk = torch.empty(c.B, c.Hkv, c.S, c.D, dtype=torch.bfloat16, device="cuda")
+    dk = torch.empty(c.B, c.Hkv, c.k.shape[2], c.D, dtype=torch.bfloat16, device="cuda")
     dv = torch.empty_like(dk)
     if dbg:
         dash.attn_bwd_debug(c.q, c.k, c.v, c.o, c.do, c.lse, dq, dk, dv, c.causal, sched, window=window, **dbg)
@@ -102,7 +102,8 @@ def test_full_size(name):
         if sched == "atomic_nondet":
             got = nd
         else:
-            log = torch.full((c.B * c.Hq * c.n, c.n), -1, dtype=torch.int32, device="cuda")
+            nkv = (c.k.shape[2] + 127) // 128
+            log = torch.full((c.B * c.Hq * c.n, nkv), -1, dtype=torch.int32, device="cuda")
             got = run_full(c, sched, w.window, order_log=log)
             again = run_full(c, sched, w.window)
             for a, b in zip(got, again):
@@ -110,6 +111,8 @@ def test_full_size(name):
             if w.window:
                 _, turns, _ = dash.sim_schedule(sched, True, c.B, c.Hq, c.Hkv, c.n, dash.num_ctas(),
                                                 band=band_tiles(w.window))
+            elif w.Skv:
+                _, turns, _ = dash.sim_schedule(sched, False, c.B, c.Hq, c.Hkv, c.n, dash.num_ctas(), nkv=nkv)
             else:
                 turns = sim_turns(c, sched)
             np.testing.assert_array_equal(log.cpu().numpy(), turns)
@@ -135,9 +138,12 @@ def test_full_size(name):
                 ref_q.append(ref[:nr])
             rel, _ = err(np.concatenate(got_q), np.concatenate(ref_q))
             assert rel <= REL_L2, (sched, "dq", b, hk, rel)
-            rk, rv = A.dkv_rows(qs, ks, vs, o_ex, dos, lse_ex, w.causal, 0, 0, rows, window=w.window)
-            for nm, g, ref in (("dk", dk[b, hk, rows], rk), ("dv", dv[b, hk, rows], rv)):
+            Skv = k.shape[2]   # key rows for dK/dV (the key length may differ)
+            krnd, kedge = random_rows(Skv, seed=b * 1000 + hk + 7), edge_rows(Skv)
+            krows, knr = krnd + kedge, len(krnd)
+            rk, rv = A.dkv_rows(qs, ks, vs, o_ex, dos, lse_ex, w.causal, 0, 0, krows, window=w.window)
+            for nm, g, ref in (("dk", dk[b, hk, krows], rk), ("dv", dv[b, hk, krows], rv)):
                 g = g.float().cpu().numpy().astype(np.float64)
                 assert np.abs(g - ref).max() <= MAX_ABS, (sched, nm + " max-abs", b, hk)
-                rel, _ = err(g[:nr], ref[:nr])
+                rel, _ = err(g[:knr], ref[:knr])
                 assert rel <= REL_L2, (sched, nm, b, hk, rel)

@@ -128,7 +128,8 @@ int validate_shape(int B, int Hq, int Hkv, int S, int D, int causal, int schedul
 
 int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const dash_bf16* o, const dash_bf16* dO,
              const float* lse, float* dq, dash_bf16* dk, dash_bf16* dv, int B, int Hq, int Hkv, int S, int D,
-             int causal, int schedule, cudaStream_t stream, const dash_debug_opts* dbg, int window = 0) {
+             int causal, int schedule, cudaStream_t stream, const dash_debug_opts* dbg, int window = 0,
+             int Skv = 0) {
     const void* ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv};
     for (const void* ptr : ptrs)
         if (!aligned16(ptr)) return DASH_ERR_ARG;
@@ -138,6 +139,9 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
     if (window >= S) window = 0;   // a window that covers the sequence is the causal mask
     const int win = window ? band_tiles(window) : 0;
     if (win && dbg && dbg->ranks_host) return DASH_ERR_ARG;   // the table check knows no window
+    if (Skv == 0) Skv = S;
+    if (Skv < 0 || (Skv != S && (causal || (dbg && dbg->ranks_host))) || (Skv + 127) / 128 > 65535)
+        return DASH_ERR_ARG;   // different lengths: full mask only
     if (schedule == kAuto) schedule = select_schedule(D, causal);
     int dev = 0;
     if ((rc = check_device(&dev))) return rc;
@@ -147,9 +151,10 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
     if (rc) return DASH_ERR_CUDA;
 
     const int n = (S + 127) / 128;   // the last tile may be partial
-    const Shape sh{B, Hq, Hkv, n, Hq / Hkv, causal, schedule, win};
+    const int nkv = (Skv + 127) / 128;
+    const Shape sh{B, Hq, Hkv, n, Hq / Hkv, causal, schedule, win, nkv == n ? 0 : nkv};
     const long long tiles = (long long)B * Hq * n;
-    const long long entries = tiles * n;
+    const long long entries = tiles * nkv;
     const long long ntasks = num_tasks(sh);
     const bool use_table = dbg && dbg->ranks_host;
     if (use_table && !is_static(schedule)) return DASH_ERR_ARG;
@@ -170,14 +175,15 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
             return DASH_ERR_CUDA;
         ranks = (const uint16_t*)ws->dbg_ranks.p;
     } else if (is_static(schedule)) {
-        const long long key[8] = {B, Hq, Hkv, n, causal, is_symmetric(sh) ? kSymmetric : kShift, P, win};
+        const long long key[8] = {B, Hq, Hkv, n, causal, is_symmetric(sh) ? kSymmetric : kShift, P,
+                                  (long long)win * 65536 + nkv};
         if (memcmp(key, ws->table_key, sizeof(key)) != 0) {
             if (ws->ranks.ensure((size_t)entries * sizeof(uint16_t)) ||
                 ws->time.ensure((size_t)entries * sizeof(uint32_t)) ||
                 ws->task_start.ensure((size_t)ntasks * sizeof(uint32_t)))
                 return DASH_ERR_NOMEM;
             if (launch_build_ranks(B, Hq, Hkv, n, causal, schedule, P, (uint16_t*)ws->ranks.p,
-                                   (uint32_t*)ws->time.p, (uint32_t*)ws->task_start.p, stream, win))
+                                   (uint32_t*)ws->time.p, (uint32_t*)ws->task_start.p, stream, win, sh.nk))
                 return DASH_ERR_CUDA;
             memcpy(ws->table_key, key, sizeof(key));
         }
@@ -192,8 +198,8 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
 
     BwdParams prm;
     memset(&prm, 0, sizeof(prm));
-    if (make_tmap_3d(&prm.tm_q, q, (long long)B * Hq, S, D) || make_tmap_3d(&prm.tm_k, k, (long long)B * Hkv, S, D) ||
-        make_tmap_3d(&prm.tm_v, v, (long long)B * Hkv, S, D) || make_tmap_3d(&prm.tm_do, dO, (long long)B * Hq, S, D))
+    if (make_tmap_3d(&prm.tm_q, q, (long long)B * Hq, S, D) || make_tmap_3d(&prm.tm_k, k, (long long)B * Hkv, Skv, D) ||
+        make_tmap_3d(&prm.tm_v, v, (long long)B * Hkv, Skv, D) || make_tmap_3d(&prm.tm_do, dO, (long long)B * Hq, S, D))
         return DASH_ERR_CUDA;
     prm.lse = lse;
     prm.delta = (const float*)ws->delta.p;
@@ -230,6 +236,9 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
     prm.scale_log2e = prm.scale * kLog2e;
     prm.window = window;
     prm.win = win;
+    prm.Skv = Skv;
+    prm.nk = sh.nk;
+    prm.nkv = nkv;
     if (dbg && dbg->kernel_event_begin &&
         cudaEventRecord((cudaEvent_t)dbg->kernel_event_begin, stream) != cudaSuccess)
         return DASH_ERR_CUDA;
@@ -313,11 +322,11 @@ int dash_attn_bwd_debug(const dash_bf16* q, const dash_bf16* k, const dash_bf16*
                         int Hq, int Hkv, int S, int D, int causal, int schedule, dash_stream_t stream,
                         const dash_debug_opts* opts) {
     return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, S, D, causal, schedule, (cudaStream_t)stream,
-                    opts, opts ? opts->window : 0);
+                    opts, opts ? opts->window : 0, opts ? opts->skv : 0);
 }
 
 static int fwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, dash_bf16* o, float* lse, int B,
-                    int Hq, int Hkv, int S, int D, int causal, int window, dash_stream_t stream_) {
+                    int Hq, int Hkv, int S, int D, int causal, int window, dash_stream_t stream_, int Skv = 0) {
     cudaStream_t stream = (cudaStream_t)stream_;
     const void* ptrs[] = {q, k, v, o, lse};
     for (const void* ptr : ptrs)
@@ -326,13 +335,15 @@ static int fwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, 
     if (rc) return rc;
     if (window < 0 || (window > 0 && !causal)) return DASH_ERR_ARG;
     if (window >= S) window = 0;
+    if (Skv == 0) Skv = S;
+    if (Skv < 0 || (Skv != S && causal) || (Skv + 127) / 128 > 65535) return DASH_ERR_ARG;
     int dev = 0;
     if ((rc = check_device(&dev))) return rc;
     Workspace* ws = get_ws(dev, stream);
     if (ws->ints.ensure((size_t)kIntHeader * sizeof(int))) return DASH_ERR_NOMEM;
     if (cudaMemsetAsync(ws->ints.p, 0, 8 * sizeof(int), stream) != cudaSuccess) return DASH_ERR_CUDA;
     rc = launch_fwd(q, k, v, o, lse, (int*)ws->ints.p, B, Hq, Hkv, S, D, causal, window, g_timeout_ns.load(),
-                    stream);
+                    stream, Skv);
     if (rc == -1) return DASH_ERR_ARG;
     return rc ? DASH_ERR_CUDA : DASH_OK;
 }
@@ -346,6 +357,20 @@ int dash_attn_fwd_window(const dash_bf16* q, const dash_bf16* k, const dash_bf16
                          int B, int Hq, int Hkv, int S, int D, int window, dash_stream_t stream) {
     if (window < 1) return DASH_ERR_ARG;
     return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, S, D, 1, window, stream);
+}
+
+int dash_attn_fwd_cross(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, dash_bf16* o, float* lse,
+                        int B, int Hq, int Hkv, int Sq, int Skv, int D, dash_stream_t stream) {
+    if (Skv < 1) return DASH_ERR_ARG;
+    return fwd_impl(q, k, v, o, lse, B, Hq, Hkv, Sq, D, 0, 0, stream, Skv);
+}
+
+int dash_attn_bwd_cross(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const dash_bf16* o,
+                        const dash_bf16* dO, const float* lse, float* dq, dash_bf16* dk, dash_bf16* dv, int B,
+                        int Hq, int Hkv, int Sq, int Skv, int D, int schedule, dash_stream_t stream) {
+    if (Skv < 1) return DASH_ERR_ARG;
+    return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Sq, D, 0, schedule, (cudaStream_t)stream, nullptr, 0,
+                    Skv);
 }
 
 int dash_attn_bwd_window(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const dash_bf16* o,

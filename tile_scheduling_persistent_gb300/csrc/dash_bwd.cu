@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int slot = p.cta_perm ? p.cta_perm[blockIdx.x] : (int)blockIdx.x;
-    const Shape sh{p.B, p.Hq, p.Hkv, p.n, p.G, p.causal, p.sched, p.win};
+    const Shape sh{p.B, p.Hq, p.Hkv, p.n, p.G, p.causal, p.sched, p.win, p.nk};
     const bool ordered = is_ordered(p.sched);
 
     // Each warpgroup first re-sizes its registers (all four warps execute the
@@ -223,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                     d.kv = v.kv;
                     d.flags = (first ? kKvFirst : 0) | (last ? kKvLast : 0) |
                               ((p.causal && v.q == v.kv) ? kDiag : 0) |
-                              ((kMasked && (((p.S & 127) && (v.q == p.n - 1 || v.kv == p.n - 1)) ||
+                              ((kMasked && (((p.S & 127) && v.q == p.n - 1) || ((p.Skv & 127) && v.kv == p.nkv - 1) ||
                                             (p.window && 128 * (v.q - v.kv) + 127 >= p.window)))
                                    ? kPartial : 0);   // partial last tile, or the far edge of the window
                     d.rank = rank;
@@ -425,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
             float P[64];
             unsigned long long tc0 = kProf ? clock64() : 0ull;
             softmax_64<kMasked || D == 64>(tmem + lane_off + C::COL_S, c0, lse2_a, lse2_b, p.scale_log2e, (d.flags & (kDiag | kPartial)) != 0,
-                       (d.flags & kDiag) != 0, row, p.S - d.kv * 128, p.S - d.q * 128,
+                       (d.flags & kDiag) != 0, row, p.Skv - d.kv * 128, p.S - d.q * 128,
                        p.window ? p.window - 128 * (d.q - d.kv) : (1 << 30), P);
             prof_add(c, kRoleSoftmax, 8, tc0);
             ptx::tc_fence_before();
@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
             if (rec) trace_ev<kProf>(p, pp, EV_DR_DQ_EMPTY);
             const int tile = (d.b * p.Hq + d.hq) * p.n + d.q;
             if (p.partials) {
-                float* gp = p.partials + ((size_t)tile * p.n + d.kv) * 128 * D;
+                float* gp = p.partials + ((size_t)tile * p.nkv + d.kv) * 128 * D;
 #pragma unroll
                 for (int j = 0; j < D / 8; ++j) {
                     *reinterpret_cast<float2*>(gp + (size_t)qa * D + 8 * j + ca) =
@@ -535,13 +535,13 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                     prof_add(c, kRoleDrain, 8, t0);
                     if (good && st == 0 && p.order_log) {
                         const int s = atomicAdd(p.logcnt + tile, 1);
-                        if (s >= 0 && s < p.n) p.order_log[(size_t)tile * p.n + s] = d.kv;
+                        if (s >= 0 && s < p.nkv) p.order_log[(size_t)tile * p.nkv + s] = d.kv;
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, good, 0) != 0;
             } else if (st == 0 && p.order_log && lane == 0) {
                 const int s = atomicAdd(p.logcnt + tile, 1);
-                if (s >= 0 && s < p.n) p.order_log[(size_t)tile * p.n + s] = d.kv;
+                if (s >= 0 && s < p.nkv) p.order_log[(size_t)tile * p.nkv + s] = d.kv;
             }
             if (!ok) break;
             if (rec) trace_ev<kProf>(p, pp, EV_DR_TURN);
@@ -573,8 +573,8 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                 if (!waitw(BAR(B_ACC_FULL), (uint32_t)(kvc & 1), c, kRoleDrain, (int)pp, 2)) break;
                 ptx::tc_fence_after();
                 const int krow = 32 * sub + lane;
-                const bool krow_ok = !kMasked || d.kv * 128 + krow < p.S;   // rows past S are not stored
-                const size_t grow = ((size_t)(d.b * p.Hkv + d.hkv) * p.S + (size_t)d.kv * 128 + krow) * D;
+                const bool krow_ok = !kMasked || d.kv * 128 + krow < p.Skv;   // rows past S_kv are not stored
+                const size_t grow = ((size_t)(d.b * p.Hkv + d.hkv) * p.Skv + (size_t)d.kv * 128 + krow) * D;
                 __nv_bfloat16* out = (half == 0 ? p.dk : p.dv) + grow;
                 const uint32_t col = half == 0 ? C::COL_DK : C::COL_DV;
 #pragma unroll
@@ -671,7 +671,7 @@ int bwd_max_ctas(int D, int device, int* P) {
 }
 
 int launch_bwd_dispatch(int D, const BwdParams& prm, int grid, cudaStream_t stream) {
-    if ((prm.S % 128) || prm.window) {   // a partial last tile or a window: the masked instantiation
+    if ((prm.S % 128) || (prm.Skv % 128) || prm.window) {   // a partial last tile or a window: masked
         if (prm.prof)
             return D == 64 ? launch_bwd<64, true, true>(prm, grid, stream) : launch_bwd<128, true, true>(prm, grid, stream);
         return D == 64 ? launch_bwd<64, false, true>(prm, grid, stream) : launch_bwd<128, false, true>(prm, grid, stream);

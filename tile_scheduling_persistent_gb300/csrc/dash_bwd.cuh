@@ -175,6 +175,9 @@ struct BwdParams {
     float scale, scale_log2e;
     int window;                             // causal sliding window in tokens (0 = none)
     int win;                                // its tile diagonals (band_tiles), 0 = none
+    int Skv;                                // key/value length (S is the query length)
+    int nk;                                 // key/value tiles when they differ from n, else 0
+    int nkv;                                // key/value tiles per head (n or nk)
 };
 
 // ------------------------------------------------------------------ MMA issue

@@ -47,6 +47,7 @@ struct FwdParams {
     float scale_log2e;
     int window;                     // causal sliding window in tokens (0 = none)
     int win;                        // its tile diagonals (band_tiles), 0 = none
+    int Skv, nkv;                   // key/value length and tiles (S, n: the query's)
 };
 
 enum FwdBar : int {
@@ -147,7 +148,7 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
     // KV tiles j0 .. j0 + nkv - 1 (a window starts the range at its far edge);
     // loops count j from 0 and address the tile j0 + j
     const int j0 = (p.causal && p.win && qt >= p.win) ? qt - p.win + 1 : 0;
-    const int nkv = p.causal ? qt - j0 + 1 : p.n;
+    const int nkv = p.causal ? qt - j0 + 1 : p.nkv;
     const int qrow = (b * p.Hq + hq) * p.S + qt * 128;   // first row of this tile in o / lse
     const int hqi = b * p.Hq + hq, hki = b * p.Hkv + hkv;  // head indices of the 3-D tensor maps
 
@@ -288,8 +289,8 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
                 for (int k = 0; k < 128; ++k)
                     if (row - k >= wlim) x[k] = -INFINITY;
             }
-            if (kMasked && jt == p.n - 1 && (p.S & 127)) {   // keys past S of the partial last tile
-                const int lim = p.S - jt * 128;
+            if (kMasked && jt == p.nkv - 1 && (p.Skv & 127)) {   // keys past S_kv of the partial last tile
+                const int lim = p.Skv - jt * 128;
 #pragma unroll
                 for (int k = 0; k < 128; ++k)
                     if (k >= lim) x[k] = -INFINITY;
@@ -415,10 +416,12 @@ int launch_fwd_t(const FwdParams& prm, int grid, cudaStream_t stream) {
 }  // namespace
 
 int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int* status, int B, int Hq,
-               int Hkv, int S, int D, int causal, int window, unsigned long long timeout_ns, cudaStream_t stream) {
+               int Hkv, int S, int D, int causal, int window, unsigned long long timeout_ns, cudaStream_t stream,
+               int Skv) {
+    if (Skv == 0) Skv = S;
     FwdParams prm;
-    if (make_tmap_3d(&prm.tm_q, q, (long long)B * Hq, S, D) || make_tmap_3d(&prm.tm_k, k, (long long)B * Hkv, S, D) ||
-        make_tmap_3d(&prm.tm_v, v, (long long)B * Hkv, S, D))
+    if (make_tmap_3d(&prm.tm_q, q, (long long)B * Hq, S, D) || make_tmap_3d(&prm.tm_k, k, (long long)B * Hkv, Skv, D) ||
+        make_tmap_3d(&prm.tm_v, v, (long long)B * Hkv, Skv, D))
         return -2;
     prm.o = (__nv_bfloat16*)o;
     prm.lse = lse;
@@ -434,9 +437,11 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
     prm.scale_log2e = (1.0f / sqrtf((float)D)) * kLog2e;
     prm.window = window;
     prm.win = window ? band_tiles(window) : 0;
+    prm.Skv = Skv;
+    prm.nkv = (Skv + 127) / 128;
     const long long grid = (long long)B * Hq * ((S + 127) / 128);
     if (grid <= 0 || grid > 0x7fffffffll) return -1;
-    if ((S % 128) || window)
+    if ((S % 128) || (Skv % 128) || window)
         return D == 64 ? launch_fwd_t<64, true>(prm, (int)grid, stream) : launch_fwd_t<128, true>(prm, (int)grid, stream);
     return D == 64 ? launch_fwd_t<64, false>(prm, (int)grid, stream) : launch_fwd_t<128, false>(prm, (int)grid, stream);
 }

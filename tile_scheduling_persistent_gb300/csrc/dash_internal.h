@@ -24,7 +24,8 @@ int launch_build_ranks(int B, int Hq, int Hkv, int n, int causal, int sched, int
 // Attention forward (dash_fwd.cu): O bf16 [B,Hq,S,D], LSE fp32 [B,Hq,S];
 // status = the stream workspace's status word (cleared by the caller).
 int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int* status, int B, int Hq,
-               int Hkv, int S, int D, int causal, int window, unsigned long long timeout_ns, cudaStream_t stream);
+               int Hkv, int S, int D, int causal, int window, unsigned long long timeout_ns, cudaStream_t stream,
+               int Skv = 0);
 
 // Single-tile probe (dash_probe.cu).
 int run_tile_probe(const void* k, const void* v, const void* q, const void* dO, const float* lse,

@@ -147,6 +147,8 @@ extern "C" int dash_attn_bwd_noalloc(const dash_bf16* q, const dash_bf16* k, con
     prm.P = P;
     prm.scale = 1.0f / sqrtf((float)D);
     prm.scale_log2e = prm.scale * kLog2e;
+    prm.Skv = S;   // equal query and key lengths, no window
+    prm.nkv = n;
     rc = launch_bwd_dispatch(D, prm, P, stream);
     if (rc == -3) return DASH_ERR_LAUNCH;
     return rc ? DASH_ERR_CUDA : DASH_OK;

@@ -27,7 +27,7 @@ EXPORTS = (
     "dash_release_workspaces", "dash_num_ctas", "dash_sim_schedule", "dash_sim_check_ranks",
     "dash_attn_bwd_debug", "dash_debug_tile_probe", "dash_attn_bwd_noalloc", "dash_select_schedule",
     "dash_attn_fwd", "dash_sim_schedule_band", "dash_attn_bwd_window", "dash_attn_fwd_window",
-    "dash_sim_schedule_cross",
+    "dash_sim_schedule_cross", "dash_attn_bwd_cross", "dash_attn_fwd_cross",
 )
 
 
@@ -42,7 +42,7 @@ class _DebugOpts(ctypes.Structure):
                 ("start_delay_ns", ctypes.c_void_p), ("ranks_host", ctypes.c_void_p),
                 ("skip_table_check", ctypes.c_int), ("kernel_event_begin", ctypes.c_void_p),
                 ("kernel_event_end", ctypes.c_void_p), ("wait_cycles", ctypes.c_void_p),
-                ("event_trace", ctypes.c_void_p), ("window", ctypes.c_int)]
+                ("event_trace", ctypes.c_void_p), ("window", ctypes.c_int), ("skv", ctypes.c_int)]
 
 
 _lib = None
@@ -118,7 +118,15 @@ def _bwd_args(q, k, v, o, do, lse, dq, dk, dv, causal, schedule):
 
 def attn_bwd(q, k, v, o, do, lse, dq, dk, dv, causal, schedule, stream=None, window=None):
     """dq (fp32 accumulator, zeroed by the library), dk, dv (bf16) <- backward.
-    window: causal sliding window in tokens (needs causal=True), or None."""
+    window: causal sliding window in tokens (needs causal=True), or None.
+    k/v (and dk/dv) may be longer or shorter than q (full mask only)."""
+    if k.shape[2] != q.shape[2]:
+        assert not causal and window is None, "different lengths need a full mask"
+        args = _bwd_args(q, k, v, o, do, lse, dq, dk, dv, causal, schedule)
+        args[-3:-2] = [k.shape[2], q.shape[3]]   # (..., Sq, D, causal, sched) -> (..., Sq, Skv, D, sched)
+        del args[-2]
+        _check(lib().dash_attn_bwd_cross(*args, _stream(stream)), "dash_attn_bwd_cross")
+        return
     if window is not None:
         assert causal, "a sliding window needs a causal mask"
         args = _bwd_args(q, k, v, o, do, lse, dq, dk, dv, causal, schedule)
@@ -141,6 +149,7 @@ def attn_bwd_debug(q, k, v, o, do, lse, dq, dk, dv, causal, schedule, stream=Non
                    kernel_events=None, wait_cycles=None, event_trace=None, window=None):
     opts = _DebugOpts()
     opts.window = int(window) if window is not None else 0
+    opts.skv = int(k.shape[2]) if k.shape[2] != q.shape[2] else 0
     opts.wait_cycles = _ptr(wait_cycles, torch.int64)
     opts.event_trace = _ptr(event_trace, torch.int64)
     if kernel_events is not None:
@@ -190,6 +199,10 @@ def attn_fwd(q, k, v, o, lse, causal, stream=None, window=None):
     Hkv = k.shape[1]
     bf = torch.bfloat16
     ptrs = (_ptr(q, bf), _ptr(k, bf), _ptr(v, bf), _ptr(o, bf), _ptr(lse, torch.float32))
+    if k.shape[2] != S:
+        assert not causal and window is None, "different lengths need a full mask"
+        _check(lib().dash_attn_fwd_cross(*ptrs, B, Hq, Hkv, S, k.shape[2], D, _stream(stream)), "dash_attn_fwd_cross")
+        return
     if window is not None:
         assert causal, "a sliding window needs a causal mask"
         _check(lib().dash_attn_fwd_window(*ptrs, B, Hq, Hkv, S, D, int(window), _stream(stream)),

@@ -38,6 +38,7 @@ class Workload:
     sigma_do: float
     schedules: tuple
     window: int | None = None   # causal sliding window in tokens (None: none)
+    Skv: int | None = None      # key/value length when it differs from S (full masks)
 
 
 WORKLOADS = {
@@ -61,25 +62,29 @@ WORKLOADS = {
     "window_b1_hq32_hkv8_s16384_d128_w4096": Workload(
         "window_b1_hq32_hkv8_s16384_d128_w4096", True, 1, 32, 8, 16384, 128, 0.5, 1e-2,
         ("shift", "descending_q", "serialized_ascending", "atomic_nondet"), window=4096),
+    # different query and key lengths: 1K queries against 8K keys (full mask)
+    "cross_b4_h16_sq1024_skv8192_d128": Workload(
+        "cross_b4_h16_sq1024_skv8192_d128", False, 4, 16, 16, 1024, 128, 1.0, 1.0,
+        ("shift", "serialized_ascending", "descending_q", "atomic_nondet"), Skv=8192),
 }
 
 
 def make_qkvdo(B: int, Hq: int, Hkv: int, S: int, D: int, seed: int = 0,
-               sigma_qkv: float = 1.0, sigma_do: float = 1.0):
-    """Seeded bf16 (q, k, v, do) on the CPU, shapes [B,H,S,D]."""
+               sigma_qkv: float = 1.0, sigma_do: float = 1.0, Skv: int | None = None):
+    """Seeded bf16 (q, k, v, do) on the CPU, shapes [B,H,S,D] (k, v: [B,Hkv,Skv,D])."""
     g = torch.Generator(device="cpu")
     g.manual_seed(int(seed))
 
-    def draw(h, sigma):
-        x = torch.randn((B, h, S, D), generator=g, dtype=torch.float32)
+    def draw(h, sigma, L=S):
+        x = torch.randn((B, h, L, D), generator=g, dtype=torch.float32)
         return (x * sigma).to(torch.bfloat16)
 
     q = draw(Hq, sigma_qkv)
-    k = draw(Hkv, sigma_qkv)
-    v = draw(Hkv, sigma_qkv)
+    k = draw(Hkv, sigma_qkv, S if Skv is None else Skv)
+    v = draw(Hkv, sigma_qkv, S if Skv is None else Skv)
     do = draw(Hq, sigma_do)
     return q, k, v, do
 
 
 def make_workload_inputs(w: Workload, seed: int = 0):
-    return make_qkvdo(w.B, w.Hq, w.Hkv, w.S, w.D, seed, w.sigma_qkv, w.sigma_do)
+    return make_qkvdo(w.B, w.Hq, w.Hkv, w.S, w.D, seed, w.sigma_qkv, w.sigma_do, w.Skv)
