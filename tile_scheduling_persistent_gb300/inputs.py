@@ -57,6 +57,10 @@ WORKLOADS = {
     "gqa_causal_b1_hq32_hkv8_s16384_d128": Workload(
         "gqa_causal_b1_hq32_hkv8_s16384_d128", True, 1, 32, 8, 16384, 128, 0.5, 1e-2,
         ("symmetric_shift", "descending_q", "shift", "serialized_ascending", "atomic_nondet")),
+    # full mask at 16K: where the pages saw shift fall behind on H800 (remote-L2 latency)
+    "full_b1_h16_s16384_d128": Workload(
+        "full_b1_h16_s16384_d128", False, 1, 16, 16, 16384, 128, 1.0, 1.0,
+        ("shift", "serialized_ascending", "descending_q", "atomic_nondet")),
     # a causal sliding window of 4096 tokens over 16K (the band mask of the
     # Ascend plan; a Mistral-style long-context layer shape)
     "window_b1_hq32_hkv8_s16384_d128_w4096": Workload(
