@@ -106,6 +106,10 @@ enum TraceEv : int {
     EV_PR_DESC = 22, EV_PR_Q_ISSUED, EV_PR_DO_ISSUED                            // producer
 };
 static_assert(B_COUNT * 8 <= kCtlDescs, "barrier area");
+// multi-slot barriers: every range ends before the next name starts
+static_assert(B_DESC_EMPTY == B_DESC_FULL + kNDesc && B_KV_FULL == B_DESC_EMPTY + kNDesc, "descriptor slots");
+static_assert(B_Q_EMPTY == B_Q_FULL + 2 && B_DO_FULL == B_Q_EMPTY + 2 && B_DO_EMPTY == B_DO_FULL + 2 &&
+                  B_S_FULL == B_DO_EMPTY + 2, "stage slots");
 static_assert(kCtlProf + kProfSmem * 8 <= 1024, "control area");
 
 struct PairDesc {
