@@ -217,6 +217,45 @@ def time_schedule(w, sched, tensors, outs, steps, warmup, stream, kernel_events=
     return ms, kms, 3   # preprocess + persistent kernel + finalize
 
 
+class Ranks:
+    """Rank bookkeeping of `bench.py --gpus N` (one process per GPU under
+    torchrun): every rank solves an independent problem of the workload's
+    shape, so nothing is exchanged on the data path.  The timed regions are
+    bracketed by barriers, a time is the maximum over ranks, and a rate counts
+    the work of all ranks (weak scaling).  `dist` is torch.distributed with an
+    initialised process group (or None for one process); `device` is where
+    the collectives' tensors live (cuda for NCCL, cpu for gloo)."""
+
+    def __init__(self, dist=None, device="cpu"):
+        self.dist = dist
+        self.device = device
+        self.world = dist.get_world_size() if dist is not None else 1
+        self.rank = dist.get_rank() if dist is not None else 0
+
+    def barrier(self):
+        if self.dist is not None:
+            self.dist.barrier()
+
+    def max(self, x):
+        """The maximum of x over ranks (every rank gets it)."""
+        if self.dist is None:
+            return float(x)
+        import torch
+        t = torch.tensor([float(x)], dtype=torch.float64, device=self.device)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def pick_fastest(self, trials):
+        """The key of `trials` (name -> ms) with the smallest maximum over
+        ranks: the same choice on every rank, ties to the first key."""
+        worst = {k: self.max(v) for k, v in trials.items()}
+        return min(worst, key=lambda k: (worst[k], list(trials).index(k)))
+
+    def rate(self, work_per_rank, ms):
+        """Whole-job rate: the work all ranks did per second, over the slowest rank's time."""
+        return self.world * work_per_rank / (ms * 1e-3)
+
+
 def main_gpu(args):
     import torch
     from tile_scheduling_persistent_gb300 import dash
@@ -262,25 +301,21 @@ def main_gpu(args):
                           "tflops": round(flop / (ms * 1e-3) / 1e12, 2), "gpu_launches": lps * args.steps}))
         return
 
-    # pick the best deterministic schedule on a short untimed probe run
+    ranks = Ranks(dist, device)
+    # pick the best deterministic schedule on a short untimed probe run (the
+    # same pick on every rank)
     trial = {}
     for s in det:
         ms, _, _ = time_schedule(w, s, tensors, outs, 3, 2, stream)
         trial[s] = ms
-    best = min(trial, key=trial.get)
+    best = ranks.pick_fastest(trial)
     print("schedule trials (ms/step): %s" % trial, file=sys.stderr, flush=True)
 
     def barrier():
-        if dist is not None:
-            dist.barrier()
+        ranks.barrier()
         torch.cuda.synchronize()
 
-    def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    max_over_ranks = ranks.max
 
     # timed: the best deterministic schedule (whole step), clocks sampled during it
     barrier()
@@ -301,7 +336,7 @@ def main_gpu(args):
     e2e_ms = max_over_ranks(e2e["ms"])
 
     burst, sustained, src = peaks()
-    value = world * flop / (ms_det * 1e-3) / 1e12
+    value = ranks.rate(flop, ms_det) / 1e12
     kach = flop / (kms_det * 1e-3) / 1e12
     line = {
         "metric": METRIC,
@@ -321,7 +356,7 @@ def main_gpu(args):
                    "l2": "inputs larger than L2 (no flush)"},
         "pct_of_bf16_peak": round(100.0 * value / world / burst, 2),
         "det_nondet_ratio": round(ms_nd / ms_det, 4),
-        "nondet_tflops": round(world * flop / (ms_nd * 1e-3) / 1e12, 2),
+        "nondet_tflops": round(ranks.rate(flop, ms_nd) / 1e12, 2),
         "schedule_trials_ms": {k: round(v, 4) for k, v in trial.items()},
         "roofline": {"bound": "tensor", "achieved": round(kach, 2), "peak": burst, "unit": "TFLOP/s",
                      "frac": round(kach / burst, 4), "traffic": NCU_TRAFFIC.get((w.name, best)),
@@ -329,12 +364,12 @@ def main_gpu(args):
                      "kernel": "dash_bwd_kernel", "peak_source": src + " burst bf16 (cuBLAS)",
                      "kernel_ms": round(kms_det, 4), "nondet_kernel_ms": round(kms_nd, 4)},
         "clocks": clocks,
-        "e2e": {"value": round(world * flop / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+        "e2e": {"value": round(ranks.rate(flop, e2e_ms) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e_ms, 4),
                 "overlap": "double-buffered: copy-in of step k+1 and copy-out of step k-1 overlap step k"},
         "gpu_launches": lps * args.steps,
         # the forward pass that produces this step's O and LSE (not in `value`): 4*S^2*D per head, halved causal
-        "forward": {"tflops": round(world * 0.4 * flop / (fwd_ms * 1e-3) / 1e12, 2), "ms": round(fwd_ms, 4),
+        "forward": {"tflops": round(ranks.rate(0.4 * flop, fwd_ms) / 1e12, 2), "ms": round(fwd_ms, 4),
                     "kernel": "dash_fwd_kernel", "deterministic": True},
     }
     if rank == 0 and not args.no_cpu_baseline:
