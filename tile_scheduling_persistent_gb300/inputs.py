@@ -53,7 +53,7 @@ WORKLOADS = {
         ("descending_q", "symmetric_shift", "serialized_ascending", "atomic_nondet")),
     "causal_b1_h32_s16384_d64": Workload(
         "causal_b1_h32_s16384_d64", True, 1, 32, 32, 16384, 64, 1.0, 1.0,
-        ("symmetric_shift", "descending_q")),
+        ("symmetric_shift", "descending_q", "shift")),   # shift: the schedule auto selects here on GB300
     "gqa_causal_b1_hq32_hkv8_s16384_d128": Workload(
         "gqa_causal_b1_hq32_hkv8_s16384_d128", True, 1, 32, 8, 16384, 128, 0.5, 1e-2,
         ("symmetric_shift", "descending_q", "shift", "serialized_ascending", "atomic_nondet")),
