@@ -149,6 +149,26 @@ int dash_attn_fwd_cross(const dash_bf16* q, const dash_bf16* k, const dash_bf16*
 int dash_select_schedule(int B, int Hq, int Hkv, int S, int D, int causal);
 
 /*
+ * dash_head_split -- does the backward of this shape, with grouped-query
+ * heads (Hq > Hkv) on a static schedule (shift, symmetric shift, or AUTO
+ * resolving to one), run one task per query head instead of one task per
+ * key/value head group?  The pages' task is one KV tile (or symmetric pair)
+ * with every query head of its group; with few, long group tasks the last
+ * wave of the P persistent CTAs runs part-empty, so the library splits the
+ * tasks per query head when that takes more than 2% off the busiest CTA's pair
+ * count (a pure function of the shape and P).  A split run has the tasks and
+ * accumulation order of the same shape with Hkv = Hq (simulate it with
+ * dash_sim_schedule(..., Hkv = Hq, ...)); each task writes its query head's
+ * dK and dV in fp32 to a library workspace, and a second kernel sums every
+ * group's heads in ascending head order before rounding to bf16.
+ *   window: causal sliding window in tokens (0 = none); Skv: key/value length
+ *   (0 = S); P: the number of persistent CTAs (dash_num_ctas).
+ * Returns 1 (split) or 0, or DASH_ERR_ARG for a shape dash_attn_bwd rejects.
+ * Host only; needs no GPU.
+ */
+int dash_head_split(int schedule, int causal, int B, int Hq, int Hkv, int S, int D, int window, int Skv, int P);
+
+/*
  * dash_attn_bwd_preprocess -- delta[b,h,s] = sum_d dO[b,h,s,d] * O[b,h,s,d].
  *
  * The per-row statistic of the softmax backward (dS = P o (dP - delta)).
@@ -204,7 +224,11 @@ int dash_attn_bwd(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v,
  * callers that have given all device memory to their own pool allocator, or
  * that run on a latency-critical path where the implicit synchronization of
  * cudaMalloc/cudaFree is not acceptable.  The caller still provides every
- * input and output buffer.
+ * input and output buffer.  With grouped-query heads it always runs one task
+ * per key/value head group (no room for per-query-head partials), so where
+ * dash_head_split returns 1 its dK and dV bits are those of
+ * dash_attn_bwd_debug with head_split = 2, not of dash_attn_bwd (both are
+ * reproducible).
  *
  * Scratch (delta, the accumulation counters, the rank tables) comes from one
  * 8 MiB file-scope device array that every GPU loading the library keeps
@@ -357,6 +381,10 @@ typedef struct {
     /* key/value length when it differs from S (as dash_attn_bwd_cross),
      * 0 = S; needs causal = 0 and no ranks_host. */
     int skv;
+    /* grouped-query heads on shift / symmetric shift: 0 = as dash_head_split
+     * decides, 1 = one task per query head, 2 = one task per key/value head
+     * group.  Ignored with ranks_host (its table is laid out for group tasks). */
+    int head_split;
 } dash_debug_opts;
 
 /* dash_attn_bwd with debug hooks; same arguments and errors, plus

@@ -87,8 +87,11 @@ def same_bits(a: torch.Tensor, b: torch.Tensor) -> bool:
 
 
 def sim_turns(c: Case, sched):
+    """The simulator's accumulation order for the backward of case c (with
+    grouped-query heads split per query head when the library does)."""
     P = dash.num_ctas()
-    _, turns, _ = dash.sim_schedule(sched, c.causal, c.B, c.Hq, c.Hkv, c.n, P)
+    hkv = dash.task_heads(sched, c.causal, c.B, c.Hq, c.Hkv, c.S, c.D, P)
+    _, turns, _ = dash.sim_schedule(sched, c.causal, c.B, c.Hq, hkv, c.n, P)
     return turns
 
 

@@ -85,7 +85,9 @@ def test_cross_order_log_matches_simulator_and_repeats(name, sched):
     nq, nkv = (Sq + 127) // 128, (Skv + 127) // 128
     log = torch.full((B * Hq * nq, nkv), -1, dtype=torch.int32, device="cuda")
     first = run_bwd(shape, t, sched, order_log=log)
-    _, turns, _ = dash.sim_schedule(sched, False, B, Hq, Hkv, nq, dash.num_ctas(), nkv=nkv)
+    P = dash.num_ctas()
+    hkv = dash.task_heads(sched, False, B, Hq, Hkv, Sq, D, P, Skv=Skv)
+    _, turns, _ = dash.sim_schedule(sched, False, B, Hq, hkv, nq, P, nkv=nkv)
     np.testing.assert_array_equal(log.cpu().numpy(), turns)
     for _ in range(4):
         again = run_bwd(shape, t, sched)

@@ -108,11 +108,13 @@ def test_full_size(name):
             again = run_full(c, sched, w.window)
             for a, b in zip(got, again):
                 assert same_bits(a, b), sched
+            P = dash.num_ctas()
+            hkv = dash.task_heads(sched, c.causal, c.B, c.Hq, c.Hkv, c.S, c.D, P, window=w.window,
+                                  Skv=c.k.shape[2] if w.Skv else None)
             if w.window:
-                _, turns, _ = dash.sim_schedule(sched, True, c.B, c.Hq, c.Hkv, c.n, dash.num_ctas(),
-                                                band=band_tiles(w.window))
+                _, turns, _ = dash.sim_schedule(sched, True, c.B, c.Hq, hkv, c.n, P, band=band_tiles(w.window))
             elif w.Skv:
-                _, turns, _ = dash.sim_schedule(sched, False, c.B, c.Hq, c.Hkv, c.n, dash.num_ctas(), nkv=nkv)
+                _, turns, _ = dash.sim_schedule(sched, False, c.B, c.Hq, hkv, c.n, P, nkv=nkv)
             else:
                 turns = sim_turns(c, sched)
             np.testing.assert_array_equal(log.cpu().numpy(), turns)

@@ -96,7 +96,9 @@ def test_window_order_log_matches_simulator_and_repeats(name, sched):
                         order_log=log, window=W)
     code, info = dash.get_status()
     assert code == 0, (code, info)
-    _, turns, _ = dash.sim_schedule(sched, True, B, Hq, Hkv, n, dash.num_ctas(), band=band)
+    P = dash.num_ctas()
+    hkv = dash.task_heads(sched, True, B, Hq, Hkv, S, D, P, window=W)
+    _, turns, _ = dash.sim_schedule(sched, True, B, Hq, hkv, n, P, band=band)
     np.testing.assert_array_equal(log.cpu().numpy(), turns)   # the GPU added in the simulator's order
     for tile in range(B * Hq * n):
         i = tile % n

@@ -1,0 +1,53 @@
+"""The rule that splits grouped-query tasks per query head (dash_head_split),
+checked on the CPU against worker loads computed from the oracle simulator's
+own task lists (oracle/dagsim.py builds them independently of the library)."""
+import pytest
+
+from oracle import dagsim as G
+from tile_scheduling_persistent_gb300 import dash
+
+P = 152
+
+
+def busiest(schedule, B, Hq, Hkv, n, causal):
+    tasks = G.make_tasks(schedule, B, Hq, Hkv, n, causal)
+    load = [0] * P
+    for k, t in enumerate(tasks):
+        load[k % P] += len(t)
+    return max(load)
+
+
+@pytest.mark.parametrize("schedule,causal,B,Hq,Hkv,S,D", [
+    ("symmetric_shift", True, 1, 32, 8, 16384, 128),   # the LLaMA3-8B-shaped workload: split
+    ("shift", True, 1, 32, 8, 16384, 128),
+    ("shift", False, 1, 8, 2, 2048, 64),
+    ("symmetric_shift", True, 1, 8, 2, 640, 128),
+    ("shift", False, 2, 4, 2, 384, 64),
+    ("symmetric_shift", True, 8, 32, 8, 4096, 128),    # many group tasks already fill the waves
+    ("shift", False, 16, 16, 4, 8192, 128),
+])
+def test_split_follows_the_busiest_worker(schedule, causal, B, Hq, Hkv, S, D):
+    n = (S + 127) // 128
+    grouped = busiest(schedule, B, Hq, Hkv, n, causal)
+    split = busiest(schedule, B, Hq, Hq, n, causal)
+    want = split * 102 < grouped * 100
+    assert dash.head_split(schedule, causal, B, Hq, Hkv, S, D, P) == want
+
+
+def test_llama_shape_is_split_and_ungrouped_shapes_are_not():
+    assert dash.head_split("symmetric_shift", True, 1, 32, 8, 16384, 128, P)
+    assert dash.head_split("auto", True, 1, 32, 8, 16384, 128, P)
+    assert not dash.head_split("symmetric_shift", True, 4, 16, 16, 8192, 128, P)   # no groups
+    assert not dash.head_split("descending_q", True, 1, 32, 8, 16384, 128, P)     # dynamic dispatch
+    assert not dash.head_split("atomic_nondet", True, 1, 32, 8, 16384, 128, P)
+    assert dash.task_heads("symmetric_shift", True, 1, 32, 8, 16384, 128, P) == 32
+    assert dash.task_heads("descending_q", True, 1, 32, 8, 16384, 128, P) == 8
+
+
+def test_rejects_bad_shapes():
+    with pytest.raises(dash.DashError):
+        dash.head_split("shift", False, 1, 6, 4, 512, 64, P)      # Hq % Hkv != 0
+    with pytest.raises(dash.DashError):
+        dash.head_split("shift", False, 1, 4, 2, 512, 64, 0)      # no workers
+    with pytest.raises(dash.DashError):
+        dash.head_split("shift", False, 1, 4, 2, 512, 64, P, window=128)   # window needs causal

@@ -42,8 +42,10 @@ def call_noalloc(c, sched):
 
 
 def call_regular(c, sched):
+    # the allocation-free entry always runs one task per key/value head group
+    # (it has no room for per-query-head partials): compare with that layout
     dq, dk, dv = outputs(c)
-    dash.attn_bwd(c.q, c.k, c.v, c.o, c.do, c.lse, dq, dk, dv, c.causal, sched)
+    dash.attn_bwd_debug(c.q, c.k, c.v, c.o, c.do, c.lse, dq, dk, dv, c.causal, sched, head_split=False)
     dqb = torch.empty(dq.shape, dtype=torch.bfloat16, device="cuda")
     dash.dq_finalize(dq, dqb)
     torch.cuda.synchronize()

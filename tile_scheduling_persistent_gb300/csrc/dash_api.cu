@@ -71,7 +71,7 @@ struct DevBuf {
 constexpr int kIntHeader = 16;
 
 struct Workspace {
-    DevBuf delta, ints, ranks, time, task_start, dbg_ranks;
+    DevBuf delta, ints, ranks, time, task_start, dbg_ranks, part;
     long long table_key[8] = {-1, -1, -1, -1, -1, -1, -1, -1};
     void release() {
         delta.release();
@@ -80,6 +80,7 @@ struct Workspace {
         time.release();
         task_start.release();
         dbg_ranks.release();
+        part.release();
         for (auto& k : table_key) k = -1;
     }
 };
@@ -126,6 +127,31 @@ int validate_shape(int B, int Hq, int Hkv, int S, int D, int causal, int schedul
     return DASH_OK;
 }
 
+// Pairs on the busiest of P workers when the tasks of `s` are dealt round-robin.
+long long max_worker_load(const Shape& s, int P) {
+    std::vector<long long> load((size_t)P, 0);
+    const long long nt = num_tasks(s);
+    for (long long k = 0; k < nt; ++k) load[(size_t)(k % P)] += task_len(s, k);
+    long long m = 0;
+    for (long long x : load) m = x > m ? x : m;
+    return m;
+}
+
+// Grouped-query heads on a static schedule: run one task per query head
+// (instead of one per key/value head group) when that takes more than 2% off
+// the busiest worker's pair count.  With few, long group tasks the last wave
+// leaves many SMs idle (causal Hq = 32, Hkv = 8, S = 16384, symmetric shift:
+// 512 tasks of 516 pairs on 152 SMs, the busiest worker at 1.19x the mean);
+// per-head tasks fill it (2048 tasks, 1.04x).  A pure function of the shape
+// and P, like the schedule itself.
+int head_split_helps(const Shape& grouped, int P) {
+    if (grouped.G <= 1 || !is_static(grouped.sched) || P <= 0) return 0;
+    Shape split = grouped;
+    split.Hkv = grouped.Hq;
+    split.G = 1;
+    return max_worker_load(split, P) * 102 < max_worker_load(grouped, P) * 100 ? 1 : 0;
+}
+
 int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const dash_bf16* o, const dash_bf16* dO,
              const float* lse, float* dq, dash_bf16* dk, dash_bf16* dv, int B, int Hq, int Hkv, int S, int D,
              int causal, int schedule, cudaStream_t stream, const dash_debug_opts* dbg, int window = 0,
@@ -155,7 +181,15 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
 
     const int n = (S + 127) / 128;   // the last tile may be partial
     const int nkv = (Skv + 127) / 128;
-    const Shape sh{B, Hq, Hkv, n, Hq / Hkv, causal, schedule, win, nkv == n ? 0 : nkv};
+    // tasks: one per key/value head group, or one per query head (head split)
+    const Shape grouped{B, Hq, Hkv, n, Hq / Hkv, causal, schedule, win, nkv == n ? 0 : nkv};
+    int split = 0;
+    if (!(dbg && dbg->ranks_host)) {   // a supplied table is laid out for group tasks
+        const int mode = dbg ? dbg->head_split : 0;
+        split = (mode == 1) ? (grouped.G > 1 && is_static(schedule)) : (mode == 2) ? 0 : head_split_helps(grouped, P);
+    }
+    const int Ht = split ? Hq : Hkv;   // task heads
+    const Shape sh{B, Hq, Ht, n, Hq / Ht, causal, schedule, win, nkv == n ? 0 : nkv};
     const long long tiles = (long long)B * Hq * n;
     const long long entries = tiles * nkv;
     const long long ntasks = num_tasks(sh);
@@ -166,8 +200,10 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
         return DASH_ERR_DEADLOCK;
 
     Workspace* ws = get_ws(dev, stream);
+    const size_t part_elems = split ? (size_t)B * Hq * Skv * D : 0;   // per-query-head dK (then dV), fp32
     if (ws->delta.ensure((size_t)tiles * 128 * sizeof(float)) ||
-        ws->ints.ensure((size_t)(kIntHeader + (kSubTiles + 1) * tiles) * sizeof(int)))
+        ws->ints.ensure((size_t)(kIntHeader + (kSubTiles + 1) * tiles) * sizeof(int)) ||
+        (split && ws->part.ensure(2 * part_elems * sizeof(float))))
         return DASH_ERR_NOMEM;
 
     const uint16_t* ranks = nullptr;
@@ -178,14 +214,14 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
             return DASH_ERR_CUDA;
         ranks = (const uint16_t*)ws->dbg_ranks.p;
     } else if (is_static(schedule)) {
-        const long long key[8] = {B, Hq, Hkv, n, causal, is_symmetric(sh) ? kSymmetric : kShift, P,
+        const long long key[8] = {B, Hq, Ht, n, causal, is_symmetric(sh) ? kSymmetric : kShift, P,
                                   (long long)win * 65536 + nkv};
         if (memcmp(key, ws->table_key, sizeof(key)) != 0) {
             if (ws->ranks.ensure((size_t)entries * sizeof(uint16_t)) ||
                 ws->time.ensure((size_t)entries * sizeof(uint32_t)) ||
                 ws->task_start.ensure((size_t)ntasks * sizeof(uint32_t)))
                 return DASH_ERR_NOMEM;
-            if (launch_build_ranks(B, Hq, Hkv, n, causal, schedule, P, (uint16_t*)ws->ranks.p,
+            if (launch_build_ranks(B, Hq, Ht, n, causal, schedule, P, (uint16_t*)ws->ranks.p,
                                    (uint32_t*)ws->time.p, (uint32_t*)ws->task_start.p, stream, win, sh.nk))
                 return DASH_ERR_CUDA;
             memcpy(ws->table_key, key, sizeof(key));
@@ -228,10 +264,12 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
     prm.ntasks = ntasks;
     prm.B = B;
     prm.Hq = Hq;
-    prm.Hkv = Hkv;
+    prm.Hkv = Ht;
+    prm.kvh = Hkv;
+    prm.kvg = Hq / Hkv;
     prm.S = S;
     prm.n = n;
-    prm.G = Hq / Hkv;
+    prm.G = Hq / Ht;
     prm.causal = causal;
     prm.sched = schedule;
     prm.P = P;
@@ -245,12 +283,21 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
     if (dbg && dbg->kernel_event_begin &&
         cudaEventRecord((cudaEvent_t)dbg->kernel_event_begin, stream) != cudaSuccess)
         return DASH_ERR_CUDA;
+    if (split) {
+        prm.part_dk = (float*)ws->part.p;
+        prm.part_dv = prm.part_dk + part_elems;
+    }
     rc = launch_bwd_dispatch(D, prm, P, stream);
     if (rc == 0 && dbg && dbg->kernel_event_end &&
         cudaEventRecord((cudaEvent_t)dbg->kernel_event_end, stream) != cudaSuccess)
         return DASH_ERR_CUDA;
     if (rc == -3) return DASH_ERR_LAUNCH;
-    return rc ? DASH_ERR_CUDA : DASH_OK;
+    if (rc) return DASH_ERR_CUDA;
+    // one task per query head: dK, dV = the group's per-head partials, ascending head order
+    if (split && (launch_group_sum(prm.part_dk, dk, B, Hkv, Hq / Hkv, Skv, D, stream) ||
+                  launch_group_sum(prm.part_dv, dv, B, Hkv, Hq / Hkv, Skv, D, stream)))
+        return DASH_ERR_CUDA;
+    return DASH_OK;
 }
 
 }  // namespace
@@ -387,6 +434,20 @@ int dash_attn_bwd_window(const dash_bf16* q, const dash_bf16* k, const dash_bf16
 int dash_select_schedule(int B, int Hq, int Hkv, int S, int D, int causal) {
     const int rc = validate_shape(B, Hq, Hkv, S, D, causal, kAuto);
     return rc ? rc : select_schedule(D, causal);
+}
+
+int dash_head_split(int schedule, int causal, int B, int Hq, int Hkv, int S, int D, int window, int Skv, int P) {
+    int rc = validate_shape(B, Hq, Hkv, S, D, causal, schedule);
+    if (rc) return rc;
+    if (P <= 0 || window < 0 || (window > 0 && !causal)) return DASH_ERR_ARG;
+    if (Skv == 0) Skv = S;
+    if (Skv < 0 || (Skv != S && causal)) return DASH_ERR_ARG;
+    if (window >= S) window = 0;
+    if (schedule == kAuto) schedule = (Skv != S) ? kDescending : select_schedule(D, causal);
+    const int n = (S + 127) / 128, nkv = (Skv + 127) / 128;
+    const Shape grouped{B, Hq, Hkv, n, Hq / Hkv, causal, schedule, window ? band_tiles(window) : 0,
+                        nkv == n ? 0 : nkv};
+    return head_split_helps(grouped, P);
 }
 
 int dash_dq_finalize(const float* dq_accum, dash_bf16* dq, size_t numel, dash_stream_t stream) {

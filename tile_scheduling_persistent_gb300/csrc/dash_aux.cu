@@ -63,6 +63,32 @@ __global__ void finalize_tail_kernel(const float* __restrict__ src, __nv_bfloat1
     if (i < end) dst[i] = __float2bfloat16_rn(src[i]);
 }
 
+// ---------------------------------------------------------------- GQA group sum
+// out[b, hk, s, :] = bf16_rn(((part[b, hk*G] + part[b, hk*G+1]) + ...) + part[b, hk*G+G-1])
+// for the fp32 per-query-head dK / dV of a backward run with one task per
+// query head: the group's heads are added in ascending order.  One thread per
+// four consecutive elements of a key/value row (D is a multiple of 4).
+__global__ void __launch_bounds__(256) group_sum_kernel(const float4* __restrict__ part, uint2* __restrict__ out,
+                                                       long long rows_out, int G, long long head4) {
+    // head4: float4s per head (Skv * D / 4); a head's rows are contiguous
+    const long long n4 = rows_out;   // float4s in the output
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += (long long)gridDim.x * blockDim.x) {
+        const long long bh = i / head4, r = i - bh * head4;   // output head (b * Hkv + hk), offset
+        const float4* src = part + bh * G * head4 + r;
+        float4 a = src[0];
+        for (int g = 1; g < G; ++g) {
+            const float4 v = src[(long long)g * head4];
+            a.x += v.x;
+            a.y += v.y;
+            a.z += v.z;
+            a.w += v.w;
+        }
+        __nv_bfloat162 lo = __floats2bfloat162_rn(a.x, a.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(a.z, a.w);
+        out[i] = make_uint2(*reinterpret_cast<uint32_t*>(&lo), *reinterpret_cast<uint32_t*>(&hi));
+    }
+}
+
 // ---------------------------------------------------------------- ranks
 // Model time of a pair = its position in its worker's unit-step sequence
 // (worker = task % P, tasks taken in order); the accumulation rank of KV
@@ -138,6 +164,20 @@ int launch_finalize(const float* src, void* dst, size_t numel, cudaStream_t s) {
         finalize_kernel<<<(unsigned)blocks, 256, 0, s>>>((const float4*)src, (uint2*)dst, n4);
     }
     if (numel % 4) finalize_tail_kernel<<<1, 32, 0, s>>>(src, (__nv_bfloat16*)dst, n4 * 4, numel);
+    return cudaGetLastError() == cudaSuccess ? 0 : -2;
+}
+
+int launch_group_sum(const float* part, void* out, int B, int Hkv, int G, int Skv, int D, cudaStream_t s) {
+    const long long head4 = (long long)Skv * D / 4;
+    const long long n4 = (long long)B * Hkv * head4;
+    if (n4 == 0) return 0;
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    long long blocks = (n4 + 255) / 256;
+    const long long cap = (long long)sms * 8;
+    if (blocks > cap) blocks = cap;
+    group_sum_kernel<<<(unsigned)blocks, 256, 0, s>>>((const float4*)part, (uint2*)out, n4, G, head4);
     return cudaGetLastError() == cudaSuccess ? 0 : -2;
 }
 

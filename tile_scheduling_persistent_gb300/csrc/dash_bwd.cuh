@@ -149,7 +149,7 @@ constexpr int kRegsLaunch = 96;
 template <int D>
 struct Regs {
     static constexpr int kCtl = 64;
-    static constexpr int kDrain = (D == 128) ? 88 : 80;
+    static constexpr int kDrain = (D == 128) ? 96 : 80;
     static constexpr int kSoftmax = (D == 128) ? 112 : 120;
     static_assert(128 * kCtl + 256 * kDrain + 256 * kSoftmax <= kThreads * kRegsLaunch, "register split");
 };
@@ -182,6 +182,14 @@ struct BwdParams {
     int Skv;                                // key/value length (S is the query length)
     int nk;                                 // key/value tiles when they differ from n, else 0
     int nkv;                                // key/value tiles per head (n or nk)
+    // Grouped-query heads.  Hkv and G above describe the tasks (with one task
+    // per query head they are Hq and 1); kvh and kvg are the key/value heads
+    // of the tensors and the query heads per key/value head.
+    int kvh, kvg;
+    // One task per query head: fp32 [B, Hq, Skv, D] dK / dV of each query
+    // head, summed over the group afterwards; null: bf16 dk / dv directly.
+    float* part_dk;
+    float* part_dv;
 };
 
 // ------------------------------------------------------------------ MMA issue

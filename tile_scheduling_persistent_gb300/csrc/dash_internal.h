@@ -15,6 +15,10 @@ int bwd_smem_bytes(int D);
 // Auxiliary kernels (dash_aux.cu).
 int launch_preprocess(const void* o, const void* dO, float* delta, long long rows, int D, cudaStream_t s);
 int launch_finalize(const float* src, void* dst, size_t numel, cudaStream_t s);
+// dK / dV of a backward run with one task per query head: out bf16
+// [B, Hkv, Skv, D] = the fp32 part [B, Hkv*G, Skv, D] summed over each group
+// of G query heads in ascending order.
+int launch_group_sum(const float* part, void* out, int B, int Hkv, int G, int Skv, int D, cudaStream_t s);
 // Accumulation ranks of a static schedule, built on the device:
 // ranks [B*Hq*n][n] (uint16), scratch `time` [B*Hq*n][n] (uint32),
 // `task_start` [num_tasks] (uint32).

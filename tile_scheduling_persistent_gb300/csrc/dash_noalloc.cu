@@ -139,6 +139,8 @@ extern "C" int dash_attn_bwd_noalloc(const dash_bf16* q, const dash_bf16* k, con
     prm.B = B;
     prm.Hq = Hq;
     prm.Hkv = Hkv;
+    prm.kvh = Hkv;   // one task per key/value head group (no per-head partials here)
+    prm.kvg = Hq / Hkv;
     prm.S = S;
     prm.n = n;
     prm.G = Hq / Hkv;

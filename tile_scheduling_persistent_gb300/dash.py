@@ -27,7 +27,7 @@ EXPORTS = (
     "dash_release_workspaces", "dash_num_ctas", "dash_sim_schedule", "dash_sim_check_ranks",
     "dash_attn_bwd_debug", "dash_debug_tile_probe", "dash_attn_bwd_noalloc", "dash_select_schedule",
     "dash_attn_fwd", "dash_sim_schedule_band", "dash_attn_bwd_window", "dash_attn_fwd_window",
-    "dash_sim_schedule_cross", "dash_attn_bwd_cross", "dash_attn_fwd_cross",
+    "dash_sim_schedule_cross", "dash_attn_bwd_cross", "dash_attn_fwd_cross", "dash_head_split",
 )
 
 
@@ -42,7 +42,8 @@ class _DebugOpts(ctypes.Structure):
                 ("start_delay_ns", ctypes.c_void_p), ("ranks_host", ctypes.c_void_p),
                 ("skip_table_check", ctypes.c_int), ("kernel_event_begin", ctypes.c_void_p),
                 ("kernel_event_end", ctypes.c_void_p), ("wait_cycles", ctypes.c_void_p),
-                ("event_trace", ctypes.c_void_p), ("window", ctypes.c_int), ("skv", ctypes.c_int)]
+                ("event_trace", ctypes.c_void_p), ("window", ctypes.c_int), ("skv", ctypes.c_int),
+                ("head_split", ctypes.c_int)]
 
 
 _lib = None
@@ -146,9 +147,12 @@ def attn_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, causal, schedule, stream=N
 
 def attn_bwd_debug(q, k, v, o, do, lse, dq, dk, dv, causal, schedule, stream=None, order_log=None,
                    dq_partials=None, cta_perm=None, start_delay_ns=None, ranks_host=None, skip_table_check=False,
-                   kernel_events=None, wait_cycles=None, event_trace=None, window=None):
+                   kernel_events=None, wait_cycles=None, event_trace=None, window=None, head_split=None):
+    """head_split: None (the library decides), True (one task per query head)
+    or False (one task per key/value head group)."""
     opts = _DebugOpts()
     opts.window = int(window) if window is not None else 0
+    opts.head_split = 0 if head_split is None else (1 if head_split else 2)
     opts.skv = int(k.shape[2]) if k.shape[2] != q.shape[2] else 0
     opts.wait_cycles = _ptr(wait_cycles, torch.int64)
     opts.event_trace = _ptr(event_trace, torch.int64)
@@ -216,6 +220,21 @@ def select_schedule(B, Hq, Hkv, S, D, causal):
     rc = lib().dash_select_schedule(B, Hq, Hkv, S, D, int(bool(causal)))
     _check(rc if rc < 0 else 0, "dash_select_schedule")
     return {v: k for k, v in SCHEDULE_IDS.items()}[rc]
+
+
+def head_split(schedule, causal, B, Hq, Hkv, S, D, P, window=None, Skv=None):
+    """True if the backward of this shape runs one task per query head (see
+    dash_head_split); its accumulation order is then that of Hkv = Hq."""
+    rc = lib().dash_head_split(_sched(schedule), int(bool(causal)), B, Hq, Hkv, S, D, int(window or 0),
+                               int(Skv or 0), int(P))
+    _check(rc if rc < 0 else 0, "dash_head_split")
+    return rc == 1
+
+
+def task_heads(schedule, causal, B, Hq, Hkv, S, D, P, window=None, Skv=None):
+    """The Hkv to simulate a backward run with: Hq when its tasks are split per
+    query head, else Hkv."""
+    return Hq if head_split(schedule, causal, B, Hq, Hkv, S, D, P, window, Skv) else Hkv
 
 
 def num_ctas(device=None):
