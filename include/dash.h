@@ -163,8 +163,9 @@ int dash_select_schedule(int B, int Hq, int Hkv, int S, int D, int causal);
  * group's heads in ascending head order before rounding to bf16.
  *   window: causal sliding window in tokens (0 = none); Skv: key/value length
  *   (0 = S); P: the number of persistent CTAs (dash_num_ctas).
- * Returns 1 (split) or 0, or DASH_ERR_ARG for a shape dash_attn_bwd rejects.
- * Host only; needs no GPU.
+ * Only D = 128 splits (the per-head partial path is compiled into the D = 128
+ * kernel alone).  Returns 1 (split) or 0, or DASH_ERR_ARG for a shape
+ * dash_attn_bwd rejects.  Host only; needs no GPU.
  */
 int dash_head_split(int schedule, int causal, int B, int Hq, int Hkv, int S, int D, int window, int Skv, int P);
 
@@ -192,7 +193,11 @@ int dash_attn_bwd_preprocess(const dash_bf16* o, const dash_bf16* dO, float* del
  *       KV-tile partials added in the order the schedule fixes.
  *   dk, dv bf16 [B,Hkv,S,D] -- accumulated on chip per KV tile over the
  *       tile's pairs in the schedule's visit order and over the query heads
- *       of its group in ascending head order; rounded to nearest even.
+ *       of its group in ascending head order; rounded to nearest even.  When
+ *       dash_head_split returns 1 for the shape, each query head is its own
+ *       task and the group's fp32 per-head results are added in ascending
+ *       head order by a second kernel instead (workspace: 2 x B*Hq*S*D*4
+ *       bytes).
  * schedule: a dash_schedule value (DASH_SCHED_AUTO runs the schedule
  * dash_select_schedule returns).  causal: 0 (full) or 1 (top-left causal).
  *
@@ -382,8 +387,9 @@ typedef struct {
      * 0 = S; needs causal = 0 and no ranks_host. */
     int skv;
     /* grouped-query heads on shift / symmetric shift: 0 = as dash_head_split
-     * decides, 1 = one task per query head, 2 = one task per key/value head
-     * group.  Ignored with ranks_host (its table is laid out for group tasks). */
+     * decides, 1 = one task per query head (D = 128 only), 2 = one task per
+     * key/value head group.  Ignored with ranks_host (its table is laid out
+     * for group tasks). */
     int head_split;
 } dash_debug_opts;
 

@@ -15,7 +15,7 @@ pytestmark = pytest.mark.gpu
 SHAPES = {
     # name: (B, Hq, Hkv, S, D, causal, schedule)
     "causal_s640_d128_g4_sym": (1, 8, 2, 640, 128, True, "symmetric_shift"),
-    "full_s384_d64_g2_shift": (2, 4, 2, 384, 64, False, "shift"),
+    "full_s384_d128_g2_shift": (2, 4, 2, 384, 128, False, "shift"),
     "causal_s333_d128_g3_shift": (1, 6, 2, 333, 128, True, "shift"),   # ragged tail
 }
 _cases = {}

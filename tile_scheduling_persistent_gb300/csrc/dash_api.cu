@@ -137,15 +137,15 @@ long long max_worker_load(const Shape& s, int P) {
     return m;
 }
 
-// Grouped-query heads on a static schedule: run one task per query head
+// Grouped-query heads on a static schedule (D = 128): run one task per query head
 // (instead of one per key/value head group) when that takes more than 2% off
 // the busiest worker's pair count.  With few, long group tasks the last wave
 // leaves many SMs idle (causal Hq = 32, Hkv = 8, S = 16384, symmetric shift:
 // 512 tasks of 516 pairs on 152 SMs, the busiest worker at 1.19x the mean);
 // per-head tasks fill it (2048 tasks, 1.04x).  A pure function of the shape
 // and P, like the schedule itself.
-int head_split_helps(const Shape& grouped, int P) {
-    if (grouped.G <= 1 || !is_static(grouped.sched) || P <= 0) return 0;
+int head_split_helps(const Shape& grouped, int P, int D) {
+    if (D != 128 || grouped.G <= 1 || !is_static(grouped.sched) || P <= 0) return 0;   // partials: D = 128
     Shape split = grouped;
     split.Hkv = grouped.Hq;
     split.G = 1;
@@ -186,7 +186,9 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
     int split = 0;
     if (!(dbg && dbg->ranks_host)) {   // a supplied table is laid out for group tasks
         const int mode = dbg ? dbg->head_split : 0;
-        split = (mode == 1) ? (grouped.G > 1 && is_static(schedule)) : (mode == 2) ? 0 : head_split_helps(grouped, P);
+        split = (mode == 1) ? (D == 128 && grouped.G > 1 && is_static(schedule))
+                : (mode == 2) ? 0
+                              : head_split_helps(grouped, P, D);
     }
     const int Ht = split ? Hq : Hkv;   // task heads
     const Shape sh{B, Hq, Ht, n, Hq / Ht, causal, schedule, win, nkv == n ? 0 : nkv};
@@ -447,7 +449,7 @@ int dash_head_split(int schedule, int causal, int B, int Hq, int Hkv, int S, int
     const int n = (S + 127) / 128, nkv = (Skv + 127) / 128;
     const Shape grouped{B, Hq, Hkv, n, Hq / Hkv, causal, schedule, window ? band_tiles(window) : 0,
                         nkv == n ? 0 : nkv};
-    return head_split_helps(grouped, P);
+    return head_split_helps(grouped, P, D);
 }
 
 int dash_dq_finalize(const float* dq_accum, dash_bf16* dq, size_t numel, dash_stream_t stream) {

@@ -239,7 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                         }
                         const uint32_t fb = BAR(B_KV_FULL);
                         ptx::mbar_arrive_expect_tx(fb, C::kKvBytes);
-                        const int hk = v.b * p.kvh + v.hq / p.kvg;   // the tensors' key/value head
+                        // the tensors' key/value head (D = 128 may run one task per query head)
+                        const int hk = (D == 128) ? v.b * p.kvh + v.hq / p.kvg : v.b * p.Hkv + v.hkv;
 #pragma unroll
                         for (int bx = 0; bx < C::kNBox; ++bx) {
                             ptx::tma_load_3d(sbase + C::OFF_K + bx * kBox, &p.tm_k, 64 * bx, v.kv * 128, hk, fb);
@@ -591,31 +592,56 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                 // every query head is its own task (fp32 partial, summed later)
                 const size_t grow = ((size_t)(d.b * p.Hkv + d.hkv) * p.Skv + (size_t)d.kv * 128 + krow) * D;
                 const uint32_t col = half == 0 ? C::COL_DK : C::COL_DV;
-                const bool f32 = p.part_dk != nullptr;
-                uint8_t* outb = f32 ? reinterpret_cast<uint8_t*>((half == 0 ? p.part_dk : p.part_dv) + grow)
-                                    : reinterpret_cast<uint8_t*>((half == 0 ? p.dk : p.dv) + grow);
+                if constexpr (D == 128) {
+                    // bf16 dK / dV, or the fp32 partials of one query head
+                    const bool f32 = p.part_dk != nullptr;
+                    uint8_t* outb = f32 ? reinterpret_cast<uint8_t*>((half == 0 ? p.part_dk : p.part_dv) + grow)
+                                        : reinterpret_cast<uint8_t*>((half == 0 ? p.dk : p.dv) + grow);
 #pragma unroll
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t v[32];
-                    ptx::tmem_ld32(tmem + kv_lanes + col + 32 * cc, v);
-                    ptx::tmem_ld_wait();
-                    if (!krow_ok) continue;
-                    if (f32) {
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t v[32];
+                        ptx::tmem_ld32(tmem + kv_lanes + col + 32 * cc, v);
+                        ptx::tmem_ld_wait();
+                        if (!krow_ok) continue;
+                        if (f32) {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e)
-                            *reinterpret_cast<uint4*>(outb + 4 * (32 * cc + 4 * e)) =
-                                make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
-                    } else {
+                            for (int e = 0; e < 8; ++e)
+                                *reinterpret_cast<uint4*>(outb + 4 * (32 * cc + 4 * e)) =
+                                    make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+                        } else {
+                            uint32_t pk[16];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            uint32_t pk[4];
-#pragma unroll
-                            for (int f = 0; f < 4; ++f) {
-                                __nv_bfloat162 h2 = __floats2bfloat162_rn(__uint_as_float(v[8 * e + 2 * f]),
-                                                                          __uint_as_float(v[8 * e + 2 * f + 1]));
-                                pk[f] = *reinterpret_cast<uint32_t*>(&h2);
+                            for (int e = 0; e < 16; ++e) {
+                                __nv_bfloat162 h2 =
+                                    __floats2bfloat162_rn(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+                                pk[e] = *reinterpret_cast<uint32_t*>(&h2);
                             }
-                            *reinterpret_cast<uint4*>(outb + 2 * (32 * cc + 8 * e)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                *reinterpret_cast<uint4*>(outb + 2 * (32 * cc + 8 * e)) =
+                                    make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
+                        }
+                    }
+                } else {
+                    // D = 64: always one task per key/value head group, bf16 out
+                    __nv_bfloat16* out = (half == 0 ? p.dk : p.dv) + grow;
+#pragma unroll
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t v[32];
+                        ptx::tmem_ld32(tmem + kv_lanes + col + 32 * cc, v);
+                        ptx::tmem_ld_wait();
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            __nv_bfloat162 h2 =
+                                __floats2bfloat162_rn(__uint_as_float(v[2 * e]), __uint_as_float(v[2 * e + 1]));
+                            pk[e] = *reinterpret_cast<uint32_t*>(&h2);
+                        }
+                        if (krow_ok) {
+#pragma unroll
+                            for (int e = 0; e < 4; ++e)
+                                *reinterpret_cast<uint4*>(out + 32 * cc + 8 * e) =
+                                    make_uint4(pk[4 * e], pk[4 * e + 1], pk[4 * e + 2], pk[4 * e + 3]);
                         }
                     }
                 }
