@@ -327,14 +327,4 @@ __device__ __forceinline__ void ds_64(uint32_t tmem_dp_lane, int c0, float delta
     }
 }
 
-__device__ __forceinline__ void store_row_sw128(uint8_t* box, int row, const uint32_t pk[32]) {
-    // 64 bf16 = 8 chunks of 16 B; chunk c lands at (c ^ (row % 8)) in the row.
-    uint8_t* rp = box + row * 128;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        *reinterpret_cast<uint4*>(rp + ((c ^ (row & 7)) << 4)) = v;
-    }
-}
-
 }  // namespace dash

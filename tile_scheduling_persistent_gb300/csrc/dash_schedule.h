@@ -18,7 +18,9 @@
 //
 // A task is one KV tile (b, hkv, j) -- or one symmetric pair -- and runs the
 // pairs of every query head of its group (ascending) back to back on one
-// CTA, so dK/dV stay in tensor memory for the whole task.
+// CTA, so dK/dV stay in tensor memory for the whole task.  (The library may
+// describe a grouped-query problem with Hkv = Hq, G = 1, i.e. one task per
+// query head, to fill the last wave; its host side then sums the group.)
 #pragma once
 #include <stdint.h>
 
