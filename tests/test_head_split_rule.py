@@ -35,6 +35,28 @@ def test_split_follows_the_busiest_worker(schedule, causal, B, Hq, Hkv, S, D):
     assert dash.head_split(schedule, causal, B, Hq, Hkv, S, D, P) == want
 
 
+@pytest.mark.parametrize("schedule,causal,B,Hq,Hkv,S,D,window,Skv", [
+    ("shift", True, 1, 32, 8, 16384, 128, 4096, None),    # causal sliding window (band tasks)
+    ("shift", True, 2, 8, 2, 3000, 128, 700, None),
+    ("shift", False, 1, 16, 4, 1024, 128, None, 8192),    # query and key lengths differ
+    ("shift", False, 4, 8, 2, 640, 128, None, 4000),
+])
+def test_split_rule_with_windows_and_cross_lengths(schedule, causal, B, Hq, Hkv, S, D, window, Skv):
+    n = (S + 127) // 128
+    band = G.band_tiles(window) if window else None
+    nkv = (Skv + 127) // 128 if Skv else None
+
+    def load(hkv):
+        tasks = G.make_tasks(schedule, B, Hq, hkv, n, causal, band, nkv)
+        w = [0] * P
+        for k, t in enumerate(tasks):
+            w[k % P] += len(t)
+        return max(w)
+
+    want = load(Hq) * 102 < load(Hkv) * 100
+    assert dash.head_split(schedule, causal, B, Hq, Hkv, S, D, P, window=window, Skv=Skv) == want
+
+
 def test_llama_shape_is_split_and_ungrouped_shapes_are_not():
     assert dash.head_split("symmetric_shift", True, 1, 32, 8, 16384, 128, P)
     assert dash.head_split("auto", True, 1, 32, 8, 16384, 128, P)
