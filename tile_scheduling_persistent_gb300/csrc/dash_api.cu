@@ -152,6 +152,22 @@ int head_split_helps(const Shape& grouped, int P, int D) {
     return max_worker_load(split, P) * 102 < max_worker_load(grouped, P) * 100 ? 1 : 0;
 }
 
+// head_split_helps, remembered per (shape, P): the decision walks every task
+// twice, which should not be paid again on every call of the same shape.
+int head_split_cached(const Shape& g, int P, int D) {
+    if (D != 128 || g.G <= 1 || !is_static(g.sched) || P <= 0) return 0;
+    static std::mutex mu;
+    static std::map<std::vector<long long>, int> memo;
+    const std::vector<long long> key{g.B, g.Hq, g.Hkv, g.n, g.causal, g.sched, g.win, g.nk, P, D};
+    std::lock_guard<std::mutex> lk(mu);
+    auto it = memo.find(key);
+    if (it != memo.end()) return it->second;
+    if (memo.size() >= 4096) memo.clear();
+    const int v = head_split_helps(g, P, D);
+    memo[key] = v;
+    return v;
+}
+
 int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const dash_bf16* o, const dash_bf16* dO,
              const float* lse, float* dq, dash_bf16* dk, dash_bf16* dv, int B, int Hq, int Hkv, int S, int D,
              int causal, int schedule, cudaStream_t stream, const dash_debug_opts* dbg, int window = 0,
@@ -188,7 +204,7 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
         const int mode = dbg ? dbg->head_split : 0;
         split = (mode == 1) ? (D == 128 && grouped.G > 1 && is_static(schedule))
                 : (mode == 2) ? 0
-                              : head_split_helps(grouped, P, D);
+                              : head_split_cached(grouped, P, D);
     }
     const int Ht = split ? Hq : Hkv;   // task heads
     const Shape sh{B, Hq, Ht, n, Hq / Ht, causal, schedule, win, nkv == n ? 0 : nkv};
