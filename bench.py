@@ -18,7 +18,6 @@ from __future__ import annotations
 
 import argparse
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -495,7 +494,6 @@ def _cpu_threads():
 def oracle_sample_step(w, heads, seed=0):
     """fp64 oracle backward on `heads` query heads of batch 0 (one key/value
     head group at a time); returns (seconds, nominal FLOP of the sample)."""
-    import numpy as np  # noqa: F401
     from oracle import attention as A
     from tile_scheduling_persistent_gb300.inputs import make_qkvdo
     G = w.Hq // w.Hkv

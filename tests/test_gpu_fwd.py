@@ -8,7 +8,7 @@ from oracle import attention as A
 from tile_scheduling_persistent_gb300 import dash
 from tile_scheduling_persistent_gb300.inputs import make_qkvdo
 
-from gpu_helpers import MAX_ABS, REL_L2, check, err, same_bits
+from gpu_helpers import check, same_bits
 
 pytestmark = pytest.mark.gpu
 

@@ -87,7 +87,7 @@ extern "C" int dash_attn_bwd_noalloc(const dash_bf16* q, const dash_bf16* k, con
     if (rc) return DASH_ERR_CUDA;
 
     const int n = (S + 127) / 128;   // the last tile may be partial
-    const Shape sh{B, Hq, Hkv, n, Hq / Hkv, causal, schedule};
+    const Shape sh{B, Hq, Hkv, n, Hq / Hkv, causal, schedule, 0, 0};   // no window, equal lengths
     const long long tiles = (long long)B * Hq * n;
     const long long entries = tiles * n;
     const long long ntasks = num_tasks(sh);
