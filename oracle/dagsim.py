@@ -49,6 +49,11 @@ lower KV index: the order in which the reductions arrive when every pair
 takes the same time, i.e. the accumulation order aligned with the execution
 schedule.
 
+Task order: head group by head group (b, hk, then the KV tile), except causal
+shift without a window, whose tasks are taken KV tile by KV tile (all groups'
+tile 0, then tile 1, ...), which balances the round-robin waves when tile j
+has n - j pairs (a GB300 choice; the pages leave the enumeration open).
+
 GQA: a task is one KV tile of head group hk; it runs the pairs of every query
 head of the group, ascending, each head's visits in the schedule's order
 (for symmetric shift: all heads' phase 1 + phase 2a of KV jp, then all
@@ -169,6 +174,11 @@ def make_tasks(schedule: str, B: int, Hq: int, Hkv: int, n: int, causal: bool, b
                 for j in range(n if nkv is None else nkv):
                     tasks.append([Pair(b, hq, i, j) for hq in heads
                                   for i in visit_q(schedule, n, causal, j, band)])
+    if schedule == "shift" and causal and band is None:
+        # causal shift is dealt KV-tile-major: task k is KV tile k // (B*Hkv) of
+        # head group k % (B*Hkv), so that each wave holds tiles of similar length
+        groups = B * Hkv
+        tasks = [tasks[g * n + j] for j in range(n) for g in range(groups)]
     return tasks
 
 

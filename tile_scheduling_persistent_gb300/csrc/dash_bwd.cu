@@ -195,7 +195,8 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
             for (;;) {
                 const int64_t k = next_task(p, slot, w);
                 const bool have = k < p.ntasks;
-                const int L = have ? task_len(sh, k) : 1;
+                const TaskRef tr = task_ref(sh, have ? k : 0);   // once per task
+                const int L = have ? task_len_at(sh, tr) : 1;
                 for (int u = 0; u < L && ok; ++u) {
                     const int ds = (int)(pc % kNDesc);
                     if (pc >= kNDesc && !wait1(BAR(B_DESC_EMPTY + ds), (uint32_t)((pc / kNDesc - 1) & 1), c,
@@ -210,9 +211,9 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                         ptx::mbar_arrive(BAR(B_DESC_FULL + ds));
                         break;
                     }
-                    const Visit v = task_visit(sh, k, u);
-                    const bool first = (u == 0) || task_visit(sh, k, u - 1).kv != v.kv;
-                    const bool last = (u == L - 1) || task_visit(sh, k, u + 1).kv != v.kv;
+                    const Visit v = visit_at(sh, tr, u);
+                    const bool first = (u == 0) || visit_at(sh, tr, u - 1).kv != v.kv;
+                    const bool last = (u == L - 1) || visit_at(sh, tr, u + 1).kv != v.kv;
                     int rank = -1;
                     if (ordered)
                         rank = p.ranks ? (int)p.ranks[rank_index(sh, v.b, v.hq, v.q, v.kv)] : v.kv - first_kv(sh, v.q);

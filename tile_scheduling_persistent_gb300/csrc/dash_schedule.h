@@ -87,27 +87,56 @@ DASH_HD int kv_len(const Shape& s, int j) {
 // whose accumulation order is ascending KV).
 DASH_HD int first_kv(const Shape& s, int q) { return (s.causal && s.win && q >= s.win) ? q - s.win + 1 : 0; }
 
-// Pairs in task k (all heads of the group).
-DASH_HD int task_len(const Shape& s, int64_t k) {
-    int t = (int)(k % tasks_per_group(s));
+// Task numbering.  Head-group-major (task k = tile k % T of group k / T)
+// except causal shift without a window, which is KV-tile-major (tile
+// k / (B*Hkv) of group k % (B*Hkv)): a causal KV tile j has n - j pairs, and
+// dealing the tasks round-robin in that order gives every wave tiles of
+// nearly equal length (busiest of 152 workers at 1.035x the mean instead of
+// 1.09x for B1 H32 S16384) and spaces the contributions to a dQ tile about a
+// wave apart.
+DASH_HD bool kv_major(const Shape& s) { return s.sched == kShift && s.causal && !s.win; }
+
+// A task's tile (or symmetric pair) and head group (b * Hkv + hkv); callers
+// that walk a task's pairs compute it once per task.  Task counts are below
+// 2^31 because B*Hq*S is.
+struct TaskRef {
+    int t, bh;
+};
+DASH_HD TaskRef task_ref(const Shape& s, int64_t k) {
+    const int kk = (int)k;
+    TaskRef r;
+    if (kv_major(s)) {
+        const int g = s.B * s.Hkv;
+        r.t = kk / g;
+        r.bh = kk - r.t * g;
+    } else {
+        const int T = tasks_per_group(s);
+        r.bh = kk / T;
+        r.t = kk - r.bh * T;
+    }
+    return r;
+}
+
+// Pairs in a task (all heads of the group).
+DASH_HD int task_len_at(const Shape& s, TaskRef r) {
+    const int t = r.t;
     if (!is_symmetric(s)) return s.G * kv_len(s, t);
     const int h = s.n / 2;
     if ((s.n & 1) && t == h) return s.G * (s.n - h);   // middle tile of an odd n
     return s.G * (s.n + 1);
 }
+DASH_HD int task_len(const Shape& s, int64_t k) { return task_len_at(s, task_ref(s, k)); }
 
 struct Visit {
     int b, hkv, hq, kv, q;   // dQ tile (b, hq, q) receives the partial of KV tile (b, hkv, kv)
 };
 
-// The u-th pair of task k, 0 <= u < task_len(s, k).
-DASH_HD Visit task_visit(const Shape& s, int64_t k, int u) {
-    const int T = tasks_per_group(s);
+// The u-th pair of a task, 0 <= u < task_len_at(s, r).
+DASH_HD Visit visit_at(const Shape& s, TaskRef r, int u) {
     Visit v;
-    const int t = (int)(k % T);
-    const int64_t bh = k / T;
-    v.hkv = (int)(bh % s.Hkv);
-    v.b = (int)(bh / s.Hkv);
+    const int t = r.t;
+    v.hkv = r.bh % s.Hkv;
+    v.b = r.bh / s.Hkv;
     const int n = s.n;
     if (!is_symmetric(s)) {
         const int j = t;
@@ -147,6 +176,7 @@ DASH_HD Visit task_visit(const Shape& s, int64_t k, int u) {
     v.q = n - 1 - (ub % Lb);
     return v;
 }
+DASH_HD Visit task_visit(const Shape& s, int64_t k, int u) { return visit_at(s, task_ref(s, k), u); }
 
 // Index of the accumulation-rank entry of pair (b, hq, q, kv).
 DASH_HD int64_t rank_index(const Shape& s, int b, int hq, int q, int kv) {
