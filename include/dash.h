@@ -138,7 +138,7 @@ int dash_attn_fwd_cross(const dash_bf16* q, const dash_bf16* k, const dash_bf16*
  *                           schedule; ascending is 26% slower)
  *   causal, D = 128      -> DASH_SCHED_SYMMETRIC_SHIFT (9% ahead of shift,
  *                           also with grouped-query heads; descending 2x slower)
- *   causal, D = 64       -> DASH_SCHED_SHIFT (10% ahead of symmetric shift)
+ *   causal, D = 64       -> DASH_SCHED_SHIFT (30% ahead of symmetric shift)
  * With a sliding window symmetric shift is shift; with different query and
  * key lengths (dash_attn_bwd_cross) AUTO runs DASH_SCHED_DESCENDING_Q
  * (measured best there).

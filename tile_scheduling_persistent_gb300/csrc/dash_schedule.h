@@ -45,7 +45,7 @@ enum Sched : int {
 // that kAuto is as reproducible as the schedule it names.  Measured on GB300
 // (kernel-only): full masks run shift (symmetric shift is the same schedule);
 // causal masks run symmetric shift at D = 128 (ahead of shift by 9%, of
-// descending by 2x) and shift at D = 64 (ahead of symmetric shift by 10%).
+// descending by 2x) and shift at D = 64 (ahead of symmetric shift by 30%).
 inline int select_schedule(int D, int causal) {
     if (!causal) return kShift;
     return D == 128 ? kSymmetric : kShift;
