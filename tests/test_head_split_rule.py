@@ -75,3 +75,23 @@ def test_rejects_bad_shapes():
         dash.head_split("shift", False, 1, 4, 2, 512, 64, 0)      # no workers
     with pytest.raises(dash.DashError):
         dash.head_split("shift", False, 1, 4, 2, 512, 64, P, window=128)   # window needs causal
+
+
+@pytest.mark.parametrize("schedule,causal,B,Hq,Hkv,n", [
+    ("shift", True, 1, 32, 32, 128),            # causal shift, dealt KV tile by KV tile
+    ("shift", True, 4, 16, 16, 64),
+    ("symmetric_shift", True, 1, 32, 8, 128),
+    ("shift", False, 4, 16, 16, 32),
+])
+def test_static_makespan_without_reduction_is_the_busiest_worker(schedule, causal, B, Hq, Hkv, n):
+    # with a zero reduction cost the DAG model's makespan of a static schedule is the
+    # pair count of its busiest worker (tasks dealt k -> k mod P in the oracle's order)
+    mk, _, _ = dash.sim_schedule(schedule, causal, B, Hq, Hkv, n, P, c=1.0, r=0.0, turn_order=False)
+    assert mk == busiest(schedule, B, Hq, Hkv, n, causal)
+
+
+def test_causal_shift_waves_are_balanced():
+    # KV-tile-major dealing keeps the busiest of 152 workers within 4% of the mean
+    tasks = G.make_tasks("shift", 1, 32, 32, 128, True)
+    mean = sum(len(t) for t in tasks) / P
+    assert busiest("shift", 1, 32, 32, 128, True) <= 1.04 * mean
