@@ -28,12 +28,39 @@ import time
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-DEFAULT_WORKLOAD = "full_b4_h16_s4096_d128"
+# The largest single-GPU configuration (causal grouped-query LLaMA3-8B layer
+# shape, S = 16384) is the headline; the other S >= 4096, D = 128
+# configurations are measured in the same run and reported under per_config.
+DEFAULT_WORKLOAD = "gqa_causal_b1_hq32_hkv8_s16384_d128"
+PER_CONFIG = ("full_b4_h16_s4096_d128", "causal_b4_h16_s8192_d128")
 METRIC = "deterministic attn-bwd TFLOP/s & % of BF16 peak; det/nondet throughput ratio"
-# DRAM bytes (read + write) of one dash_bwd_kernel launch, from one ncu capture
-# (profiles/dash_bwd_kernel_full_b4_h16_s4096_d128_shift.md).  Valid only for
-# the kernel source that capture was taken on: clear it when the kernel changes.
-NCU_TRAFFIC = {("full_b4_h16_s4096_d128", "shift"): 637692928}
+# DRAM bytes (read + write) of one dash_bwd_kernel launch per (workload,
+# schedule), each from one ncu capture, with the SHA-256 (first 16 hex digits)
+# of the kernel source it was taken on.  A figure is reported only while the
+# kernel source still has that hash; otherwise the roofline's traffic is null.
+NCU_TRAFFIC = {}
+KERNEL_SOURCES = ("tile_scheduling_persistent_gb300/csrc/dash_bwd.cu",
+                  "tile_scheduling_persistent_gb300/csrc/dash_bwd.cuh",
+                  "tile_scheduling_persistent_gb300/csrc/dash_ptx.cuh",
+                  "tile_scheduling_persistent_gb300/csrc/dash_schedule.h")
+
+
+def kernel_source_hash():
+    import hashlib
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(workload, schedule):
+    """ncu DRAM bytes per launch for this workload and schedule, or None when
+    no capture exists for the current kernel source."""
+    rec = NCU_TRAFFIC.get((workload, schedule))
+    if rec and rec[1] == kernel_source_hash():
+        return rec[0]
+    return None
 
 
 def parse():
@@ -45,6 +72,8 @@ def parse():
     ap.add_argument("--schedule", default=None, help="deterministic schedule to report (default: best of the workload's)")
     ap.add_argument("--impl", default="dash", choices=["dash", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per_config measurements of the other D = 128 configurations")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--wait-profile", action="store_true",
                     help="one step of --schedule with the kernel's per-role wait-cycle counters; prints a JSON line")
@@ -301,40 +330,15 @@ def main_gpu(args):
         return
 
     ranks = Ranks(dist, device)
-    # pick the best deterministic schedule on a short untimed probe run (the
-    # same pick on every rank)
-    trial = {}
-    for s in det:
-        ms, _, _ = time_schedule(w, s, tensors, outs, 3, 2, stream)
-        trial[s] = ms
-    best = ranks.pick_fastest(trial)
-    print("schedule trials (ms/step): %s" % trial, file=sys.stderr, flush=True)
-
-    def barrier():
-        ranks.barrier()
-        torch.cuda.synchronize()
-
-    max_over_ranks = ranks.max
-
-    # timed: the best deterministic schedule (whole step), clocks sampled during it
-    barrier()
-    with ClockSampler(local) as clk:
-        ms_det, _, lps = time_schedule(w, best, tensors, outs, args.steps, args.warmup, stream)
-    barrier()
-    ms_det = max_over_ranks(ms_det)
-    clocks = clk.summary()
-    # the dominant kernel alone (events around its launch, same stream)
-    _, kms_det, _ = time_schedule(w, best, tensors, outs, args.steps, args.warmup, stream, kernel_events=True)
-    ms_nd, kms_nd, _ = time_schedule(w, "atomic_nondet", tensors, outs, args.steps, args.warmup, stream,
-                                     kernel_events=True)
-    ms_nd = max_over_ranks(ms_nd)
+    burst, sustained, src = peaks()
+    m = measure(w, det, tensors, outs, args.steps, args.warmup, stream, ranks, sample_clocks=local)
+    best, ms_det, kms_det, ms_nd, kms_nd = m["best"], m["ms_det"], m["kms_det"], m["ms_nd"], m["kms_nd"]
 
     # end to end through the public API: host inputs in, gradients out, every step
     e2e = e2e_run(w, best, tensors, args.steps, args.warmup, stream)
-    fwd_ms = max_over_ranks(time_forward(w, tensors, args.steps, args.warmup, stream))
-    e2e_ms = max_over_ranks(e2e["ms"])
+    fwd_ms = ranks.max(time_forward(w, tensors, args.steps, args.warmup, stream))
+    e2e_ms = ranks.max(e2e["ms"])
 
-    burst, sustained, src = peaks()
     value = ranks.rate(flop, ms_det) / 1e12
     kach = flop / (kms_det * 1e-3) / 1e12
     line = {
@@ -356,21 +360,28 @@ def main_gpu(args):
         "pct_of_bf16_peak": round(100.0 * value / world / burst, 2),
         "det_nondet_ratio": round(ms_nd / ms_det, 4),
         "nondet_tflops": round(ranks.rate(flop, ms_nd) / 1e12, 2),
-        "schedule_trials_ms": {k: round(v, 4) for k, v in trial.items()},
+        "schedule_trials_ms": {k: round(v, 4) for k, v in m["trial"].items()},
         "roofline": {"bound": "tensor", "achieved": round(kach, 2), "peak": burst, "unit": "TFLOP/s",
-                     "frac": round(kach / burst, 4), "traffic": NCU_TRAFFIC.get((w.name, best)),
+                     "frac": round(kach / burst, 4), "traffic": traffic_for(w.name, best),
                      "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
-                     "kernel": "dash_bwd_kernel", "peak_source": src + " burst bf16 (cuBLAS)",
+                     "kernel": "dash_bwd_kernel", "kernel_source": kernel_source_hash(),
+                     "peak_source": src + " burst bf16 (cuBLAS)",
                      "kernel_ms": round(kms_det, 4), "nondet_kernel_ms": round(kms_nd, 4)},
-        "clocks": clocks,
+        "clocks": m["clocks"],
         "e2e": {"value": round(ranks.rate(flop, e2e_ms) / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"], "ms_per_step": round(e2e_ms, 4),
                 "overlap": "double-buffered: copy-in of step k+1 and copy-out of step k-1 overlap step k"},
-        "gpu_launches": lps * args.steps,
+        "gpu_launches": m["launches"] * args.steps,
         # the forward pass that produces this step's O and LSE (not in `value`): 4*S^2*D per head, halved causal
         "forward": {"tflops": round(ranks.rate(0.4 * flop, fwd_ms) / 1e12, 2), "ms": round(fwd_ms, 4),
                     "kernel": "dash_fwd_kernel", "deterministic": True},
     }
+    if args.workload == DEFAULT_WORKLOAD and not args.no_per_config:
+        del tensors, outs, dq, dqb, dk, dv
+        torch.cuda.empty_cache()
+        line["per_config"] = {}
+        for name in PER_CONFIG:
+            line["per_config"][name] = per_config(WORKLOADS[name], args, stream, ranks, rank, device, burst)
     if rank == 0 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, args.cpu_seconds)
     if rank == 0:
@@ -378,6 +389,63 @@ def main_gpu(args):
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
+
+
+def measure(w, det, tensors, outs, steps, warmup, stream, ranks, sample_clocks=None):
+    """Pick the fastest deterministic schedule of `det` on a short untimed
+    trial (the same pick on every rank), then time it and atomic_nondet
+    through the same public call (dash_attn_bwd + dash_dq_finalize per step),
+    each bracketed by barriers, and the persistent kernel alone (events
+    around its launch).  Times are maxima over ranks."""
+    import torch
+    trial = {}
+    for s in det:
+        ms, _, _ = time_schedule(w, s, tensors, outs, 3, 2, stream)
+        trial[s] = ms
+    best = ranks.pick_fastest(trial)
+    print("%s schedule trials (ms/step): %s" % (w.name, trial), file=sys.stderr, flush=True)
+
+    def timed(sched):
+        ranks.barrier()
+        torch.cuda.synchronize()
+        ms, _, lps = time_schedule(w, sched, tensors, outs, steps, warmup, stream)
+        ranks.barrier()
+        return ranks.max(ms), lps
+
+    clocks = None
+    if sample_clocks is not None:
+        with ClockSampler(sample_clocks) as clk:
+            ms_det, lps = timed(best)
+        clocks = clk.summary()
+    else:
+        ms_det, lps = timed(best)
+    ms_nd, _ = timed("atomic_nondet")
+    _, kms_det, _ = time_schedule(w, best, tensors, outs, steps, warmup, stream, kernel_events=True)
+    _, kms_nd, _ = time_schedule(w, "atomic_nondet", tensors, outs, steps, warmup, stream, kernel_events=True)
+    return {"best": best, "trial": trial, "ms_det": ms_det, "ms_nd": ms_nd, "kms_det": ranks.max(kms_det),
+            "kms_nd": ranks.max(kms_nd), "clocks": clocks, "launches": lps}
+
+
+def per_config(w, args, stream, ranks, rank, device, burst):
+    """value / det_nondet_ratio / kernel_ms / frac of another configuration,
+    timed like the headline (inputs resident, same calls, max over ranks)."""
+    import torch
+    tensors = gpu_inputs(w, seed=rank, device=device)
+    outs = (torch.empty(w.B, w.Hq, w.S, w.D, dtype=torch.float32, device=device),
+            torch.empty(w.B, w.Hq, w.S, w.D, dtype=torch.bfloat16, device=device),
+            torch.empty(w.B, w.Hkv, w.Skv or w.S, w.D, dtype=torch.bfloat16, device=device),
+            torch.empty(w.B, w.Hkv, w.Skv or w.S, w.D, dtype=torch.bfloat16, device=device))
+    det = [s for s in w.schedules if s != "atomic_nondet"]
+    m = measure(w, det, tensors, outs, args.steps, args.warmup, stream, ranks)
+    flop = flops_nominal(w.B, w.Hq, w.S, w.D, w.causal, w.window, w.Skv)
+    kach = flop / (m["kms_det"] * 1e-3) / 1e12
+    out = {"value": round(ranks.rate(flop, m["ms_det"]) / 1e12, 2), "unit": "TFLOP/s", "schedule": m["best"],
+           "ms_per_step": round(m["ms_det"], 4), "det_nondet_ratio": round(m["ms_nd"] / m["ms_det"], 4),
+           "nondet_tflops": round(ranks.rate(flop, m["ms_nd"]) / 1e12, 2), "kernel_ms": round(m["kms_det"], 4),
+           "frac": round(kach / burst, 4), "traffic": traffic_for(w.name, m["best"])}
+    del tensors, outs
+    torch.cuda.empty_cache()
+    return out
 
 
 WAIT_SITES = {
@@ -491,34 +559,88 @@ def _cpu_threads():
         return os.cpu_count() or 1
 
 
-def oracle_sample_step(w, heads, seed=0):
-    """fp64 oracle backward on `heads` query heads of batch 0 (one key/value
-    head group at a time); returns (seconds, nominal FLOP of the sample)."""
+def oracle_sample_inputs(w, seed=0):
+    """One query head (with its key/value head) of the workload's shape, and
+    its exact fp64 forward (O, LSE): the unit the oracle is timed on."""
     from oracle import attention as A
     from tile_scheduling_persistent_gb300.inputs import make_qkvdo
-    G = w.Hq // w.Hkv
-    groups = max(1, heads // G)
-    q, k, v, do = make_qkvdo(1, groups * G, groups, w.S, w.D, seed, w.sigma_qkv, w.sigma_do, w.Skv)
+    q, k, v, do = make_qkvdo(1, 1, 1, w.S, w.D, seed, w.sigma_qkv, w.sigma_do, w.Skv)
     o, lse = A.attn_fwd(q, k, v, w.causal, row_block=2048, workers=_cpu_threads(), window=w.window)
+    return q, k, v, do, o, lse
+
+
+def oracle_sample_step(w, inputs):
+    """fp64 oracle backward of one query head; returns (seconds, nominal FLOP)."""
+    from oracle import attention as A
+    q, k, v, do, o, lse = inputs
     t0 = time.perf_counter()
     A.attn_bwd(q, k, v, o, do, lse, w.causal, row_block=2048, workers=_cpu_threads(), window=w.window)
     dt = time.perf_counter() - t0
-    return dt, flops_nominal(1, groups * G, w.S, w.D, w.causal, w.window, w.Skv)
+    return dt, flops_nominal(1, 1, w.S, w.D, w.causal, w.window, w.Skv)
 
 
 def cpu_baseline(w, budget_s):
-    G = w.Hq // w.Hkv
     total_t = total_f = 0.0
     heads = 0
     while total_t < budget_s and heads < w.B * w.Hq:
-        dt, f = oracle_sample_step(w, G, seed=heads)
+        dt, f = oracle_sample_step(w, oracle_sample_inputs(w, seed=heads))
         total_t += dt
         total_f += f
-        heads += G
-    return {"value": round(total_f / total_t / 1e12, 6), "unit": "TFLOP/s", "cores": _cpu_threads(),
-            "kind": "oracle",
-            "sample": "%d of %d query heads (batch 0, S=%d, D=%d, %s), fp64 NumPy backward, %.1f s" % (
-                heads, w.B * w.Hq, w.S, w.D, "causal" if w.causal else "full", total_t)}
+        heads += 1
+    out = {"value": round(total_f / total_t / 1e12, 6), "unit": "TFLOP/s", "cores": _cpu_threads(),
+           "kind": "oracle",
+           "sample": "%d of %d query heads (S=%d, D=%d, %s), fp64 NumPy backward, %.1f s" % (
+               heads, w.B * w.Hq, w.S, w.D, "causal" if w.causal else "full", total_t)}
+    one = {}
+    for name, heads in ONE_CORE_SAMPLES:
+        r = one_core_oracle(name, heads)
+        if r is not None:
+            one[name] = r
+    if one:
+        out["one_core"] = one
+    return out
+
+
+# One-core oracle figures: (workload, query heads timed) -- the whole parity
+# workload and one head of the full-mask S = 4096 workload.
+ONE_CORE_SAMPLES = (("full_b1_h2_s512_d64", 2), ("full_b4_h16_s4096_d128", 1))
+
+_ONE_CORE_CHILD = """
+import json, os, sys, time
+sys.path.insert(0, %r)
+try:
+    os.sched_setaffinity(0, {sorted(os.sched_getaffinity(0))[0]})
+except Exception:
+    pass
+from oracle import attention as A
+from tile_scheduling_persistent_gb300.inputs import WORKLOADS, make_qkvdo
+w = WORKLOADS[%r]
+heads = %d
+q, k, v, do = make_qkvdo(1, heads, heads, w.S, w.D, 0, w.sigma_qkv, w.sigma_do)
+o, lse = A.attn_fwd(q, k, v, w.causal, row_block=1024)
+t0 = time.perf_counter()
+A.attn_bwd(q, k, v, o, do, lse, w.causal, row_block=1024)
+dt = time.perf_counter() - t0
+f = 10.0 * w.S * w.S * w.D * heads / (2 if w.causal else 1)
+print(json.dumps({"seconds": dt, "flop": f}))
+"""
+
+
+def one_core_oracle(name, heads):
+    """The fp64 oracle backward on `heads` query heads of workload `name`, in a
+    child process pinned to one core with every BLAS pool at one thread."""
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS",
+                "VECLIB_MAXIMUM_THREADS", "NUMEXPR_NUM_THREADS"):
+        env[var] = "1"
+    try:
+        r = subprocess.run([sys.executable, "-c", _ONE_CORE_CHILD % (ROOT, name, heads)], env=env,
+                           capture_output=True, text=True, timeout=300)
+        d = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception:
+        return None
+    return {"value": round(d["flop"] / d["seconds"] / 1e12, 6), "unit": "TFLOP/s", "cores": 1,
+            "sample": "%d query head(s), fp64 NumPy backward, %.2f s" % (heads, d["seconds"])}
 
 
 def main_reference(args):
@@ -527,12 +649,12 @@ def main_reference(args):
     if rank != 0:
         return
     w = WORKLOADS[args.workload]
-    G = w.Hq // w.Hkv
+    inputs = oracle_sample_inputs(w, seed=0)   # input synthesis, untimed
     for _ in range(args.warmup):
-        oracle_sample_step(w, G)
+        oracle_sample_step(w, inputs)
     times, flops = [], []
-    for i in range(args.steps):
-        dt, f = oracle_sample_step(w, G, seed=i)
+    for _ in range(args.steps):
+        dt, f = oracle_sample_step(w, inputs)
         times.append(dt)
         flops.append(f)
     value = sum(flops) / sum(times) / 1e12
@@ -553,7 +675,8 @@ def main_reference(args):
         "config": {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "S": w.S, "D": w.D,
                    "causal": w.causal},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": _cpu_threads(), "kind": "oracle",
-                         "sample": "each step: %d query heads (one key/value group) of batch 0, fp64 backward" % G},
+                         "sample": "each step: the fp64 backward of one query head (S=%d, D=%d) of the workload" % (
+                             w.S, w.D)},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

@@ -172,11 +172,16 @@ int dash_head_split(int schedule, int causal, int B, int Hq, int Hkv, int S, int
 /*
  * dash_attn_bwd_preprocess -- delta[b,h,s] = sum_d dO[b,h,s,d] * O[b,h,s,d].
  *
- * The per-row statistic of the softmax backward (dS = P o (dP - delta)).
- * o, dO: bf16 [B,Hq,S,D]; delta: fp32 [B,Hq,S] written by the call.  Each row
- * is summed in fp32 in one fixed order, so the result is bitwise
- * reproducible.  Returns DASH_ERR_ARG on null/misaligned pointers or bad
- * sizes (any S > 0), DASH_ERR_CUDA on launch
+ * The per-row statistic of the softmax backward (dS = P o (dP - delta)),
+ * consumed by every tile pair of the backward pass whose dQ accumulation the
+ * gist.science DASH summary (section 1) orders.  The pages do not print it:
+ * it is the textbook softmax-gradient identity (rowsum of P o dP equals
+ * rowsum of dO o O), computed once per row before the tile loop.
+ * o, dO: bf16 [B,Hq,S,D]; delta: fp32 [B,Hq,S] written by the
+ * call (caller-owned device buffers, 16-byte aligned).  Each row is summed
+ * in fp32 in one fixed order, so the result is bitwise reproducible.
+ * Returns DASH_ERR_ARG on null/misaligned pointers or bad sizes (any S > 0,
+ * D in {64, 128}), DASH_ERR_DEVICE off sm_103, DASH_ERR_CUDA on launch
  * failure.
  */
 int dash_attn_bwd_preprocess(const dash_bf16* o, const dash_bf16* dO, float* delta,
@@ -184,6 +189,17 @@ int dash_attn_bwd_preprocess(const dash_bf16* o, const dash_bf16* dO, float* del
 
 /*
  * dash_attn_bwd -- the deterministic attention backward pass.
+ *
+ * What the DASH pages define: the backward pass of softmax attention whose
+ * dQ tiles are each a sum over KV tiles that must be added in one fixed
+ * order to be reproducible (gist.science DASH summary, section 1), with each
+ * KV tile resident on one SM while it visits the Q tiles (section 2.1), and
+ * the visit / accumulation orders of the schedules in section 2.2 (descending
+ * Q-tile iteration; shift scheduling for full masks; two-phase symmetric
+ * shift for causal masks).  The gradient accumulation is fp32 with bf16
+ * storage (pwwt.cn write-up, section 3.2, mixed-precision configuration),
+ * gated per dQ tile by a counter that each contributor waits on and then
+ * advances (the write-up's release-side counter, section 3.1).
  *
  * Inputs: q, o, dO bf16 [B,Hq,S,D]; k, v bf16 [B,Hkv,S,D]; lse fp32 [B,Hq,S].
  * Outputs:
@@ -198,6 +214,7 @@ int dash_attn_bwd_preprocess(const dash_bf16* o, const dash_bf16* dO, float* del
  *       task and the group's fp32 per-head results are added in ascending
  *       head order by a second kernel instead (workspace: 2 x B*Hq*S*D*4
  *       bytes).
+ * All buffers are caller-owned device memory, contiguous, 16-byte aligned.
  * schedule: a dash_schedule value (DASH_SCHED_AUTO runs the schedule
  * dash_select_schedule returns).  causal: 0 (full) or 1 (top-left causal).
  *
@@ -224,10 +241,10 @@ int dash_attn_bwd(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v,
  * dash_attn_bwd_noalloc -- dash_attn_bwd for callers that cannot allocate.
  *
  * No counterpart on the DASH pages: this is a deployment variant.  Same
- * arguments, outputs, determinism and errors as dash_attn_bwd, but it never
- * calls cudaMalloc/cudaFree or any allocating routine.  It is meant for
- * callers that have given all device memory to their own pool allocator, or
- * that run on a latency-critical path where the implicit synchronization of
+ * arguments, outputs and determinism as dash_attn_bwd, but it never calls
+ * cudaMalloc/cudaFree or any allocating routine.  It is meant for callers
+ * that have given all device memory to their own pool allocator, or that
+ * run on a latency-critical path where the implicit synchronization of
  * cudaMalloc/cudaFree is not acceptable.  The caller still provides every
  * input and output buffer.  With grouped-query heads it always runs one task
  * per key/value head group (no room for per-query-head partials), so where
@@ -235,20 +252,29 @@ int dash_attn_bwd(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v,
  * dash_attn_bwd_debug with head_split = 2, not of dash_attn_bwd (both are
  * reproducible).
  *
- * Scratch (delta, the accumulation counters, the rank tables) comes from one
- * 8 MiB file-scope device array that every GPU loading the library keeps
- * until the process exits.  A problem needing more returns
+ * Scratch (delta, the accumulation counters, the status word, the rank
+ * tables) comes from one 8 MiB file-scope device array that every GPU loading
+ * the library keeps until the process exits.  A problem needing more returns
  * DASH_ERR_SCRATCH (roughly: B*Hq*S*4 bytes of delta plus, for the shift
  * schedules, B*Hq*(S/128)^2*6 bytes of tables must fit).
  *
- * The first call on a device looks up that device's address of the array
- * (with the device current); make that first call before any stream
- * capture.  All calls share the array and it keeps the previous call's
- * contents: each call clears what must start at zero on its stream, so
- * calls must not overlap on the GPU (different streams or host threads
- * racing on the array give undefined results).  A device-side wait that
- * times out leaves the outputs undefined; this entry point does not report
- * it through dash_get_status.
+ * Set-up: the first call on a device (or dash_noalloc_init) looks up that
+ * device's address of the array, with the device current, and loads the
+ * kernels.  Under lazy module loading (the CUDA default) that is when the
+ * driver loads the library's module and reserves the array, so do it before
+ * a pool allocator takes the whole device, before a latency-critical path and
+ * before any stream capture, or run with CUDA_MODULE_LOADING=EAGER.  After a
+ * cudaDeviceReset, call dash_noalloc_init again before the next call.
+ *
+ * All calls share the array and it keeps the previous call's contents: each
+ * call clears what must start at zero on its stream, so calls must not
+ * overlap on the GPU (different streams or host threads racing on the array
+ * give undefined results).  Device-side waits use the dash_set_timeout_ns
+ * limit; one that runs out leaves the outputs undefined and is reported by
+ * dash_get_status_noalloc (not by dash_get_status).
+ *
+ * Errors: DASH_ERR_ARG (as dash_attn_bwd), DASH_ERR_DEVICE (not sm_103),
+ * DASH_ERR_LAUNCH, DASH_ERR_SCRATCH, DASH_ERR_CUDA.
  */
 int dash_attn_bwd_noalloc(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v,
                           const dash_bf16* o, const dash_bf16* dO, const float* lse,
@@ -257,9 +283,33 @@ int dash_attn_bwd_noalloc(const dash_bf16* q, const dash_bf16* k, const dash_bf1
                           dash_stream_t stream);
 
 /*
+ * dash_noalloc_init -- set-up of dash_attn_bwd_noalloc on the current device
+ * (no counterpart on the pages): looks up the device address of its scratch
+ * array and loads every kernel it launches, so that later calls do neither.
+ * Allocates nothing itself; the driver reserves the array when it loads the
+ * module.  Calling it again refreshes the address (needed after a
+ * cudaDeviceReset).  Returns DASH_OK, DASH_ERR_DEVICE or DASH_ERR_CUDA.
+ */
+int dash_noalloc_init(void);
+
+/*
+ * dash_get_status_noalloc -- dash_get_status for dash_attn_bwd_noalloc (no
+ * counterpart on the pages): synchronizes `stream` and reports the status
+ * word of the last call on the current device, *code = DASH_OK or
+ * DASH_ERR_TIMEOUT, info[0..3] as dash_get_status (info may be NULL).  Reads
+ * the shared scratch array, so it describes whichever call last wrote it.
+ * Returns DASH_OK, DASH_ERR_ARG (code NULL), DASH_ERR_DEVICE or DASH_ERR_CUDA.
+ */
+int dash_get_status_noalloc(dash_stream_t stream, int* code, int* info);
+
+/*
  * dash_dq_finalize -- dq[i] = bf16_round_to_nearest_even(dq_accum[i]) for
- * i < numel.  dq_accum fp32, dq bf16; both device pointers, 16-byte aligned.
- * Returns DASH_ERR_ARG / DASH_ERR_CUDA.
+ * i < numel: the last step of the backward, after the fp32 accumulation of
+ * every dQ tile (pwwt.cn write-up, section 3.2: the backward's accumulations
+ * run in fp32 and tensors are stored as bf16).  dq_accum fp32 (read), dq bf16 (written); both
+ * caller-owned device pointers, 16-byte aligned, numel elements each.
+ * Returns DASH_OK (also for numel = 0), DASH_ERR_ARG (null or misaligned),
+ * DASH_ERR_DEVICE off sm_103, DASH_ERR_CUDA on launch failure.
  */
 int dash_dq_finalize(const float* dq_accum, dash_bf16* dq, size_t numel, dash_stream_t stream);
 

@@ -8,6 +8,7 @@ import pytest
 import torch
 
 from oracle import attention as A
+from oracle import dagsim
 from tile_scheduling_persistent_gb300 import dash
 
 from gpu_helpers import check, make_case, run, same_bits, sim_turns
@@ -102,7 +103,23 @@ def test_order_log_matches_simulator(name, sched):
     c = case(name)
     log = torch.full((c.B * c.Hq * c.n, c.n), -1, dtype=torch.int32, device="cuda")
     run(c, sched, order_log=log)
-    np.testing.assert_array_equal(log.cpu().numpy(), sim_turns(c, sched))
+    log = log.cpu().numpy()
+    np.testing.assert_array_equal(log, sim_turns(c, sched))
+    # and directly against the independent oracle's DAG model (no code shared
+    # with the library's simulator or the kernel)
+    np.testing.assert_array_equal(log, oracle_turns(c, sched))
+
+
+def oracle_turns(c, sched):
+    """The accumulation order of oracle.dagsim for case c, as the kernel logs
+    it: row (b*Hq + hq)*n + i lists the KV tiles added into dQ tile i."""
+    P = dash.num_ctas()
+    hkv = dash.task_heads(sched, c.causal, c.B, c.Hq, c.Hkv, c.S, c.D, P)
+    s = dagsim.build(sched, c.B, c.Hq, hkv, c.n, c.causal, P)
+    out = np.full((c.B * c.Hq * c.n, c.n), -1, dtype=np.int32)
+    for (b, hq, i), js in s.turn.items():
+        out[(b * c.Hq + hq) * c.n + i, :len(js)] = js
+    return out
 
 
 @pytest.mark.parametrize("sched", ORDERED + ["atomic_nondet"])

@@ -1,10 +1,12 @@
 """Full-size workloads: sampled parity with the fp64 oracle, bitwise
 reproducibility, order logs vs the simulator, and whole-tensor properties.
 
-At these sizes the oracle cannot produce whole tensors in seconds, so it is
-run exactly (fp64 forward for O and LSE, then the backward one row at a time)
-on sampled key/value head groups and sampled rows; the kernel is launched in
-the same configuration the benchmark times.  Heads outside the sampled
+For most of these workloads the oracle cannot produce whole tensors in
+seconds, so it is run exactly (fp64 forward for O and LSE, then the backward
+one row at a time) on sampled key/value head groups and sampled rows; the
+kernel is launched in the same configuration the benchmark times.  The
+full-mask S = 4096 workload is also compared element by element over whole
+tensors (its complete fp64 oracle takes tens of seconds on the host cores).  Heads outside the sampled
 groups get O and LSE from a plain fp32 PyTorch forward on the GPU (input
 synthesis only).  Whole tensors are checked by properties that hold at any
 size: finiteness, agreement with the unordered-atomics result of the same
@@ -149,3 +151,25 @@ def test_full_size(name):
                 assert np.abs(g - ref).max() <= MAX_ABS, (sched, nm + " max-abs", b, hk)
                 rel, _ = err(g[:knr], ref[:knr])
                 assert rel <= REL_L2, (sched, nm, b, hk, rel)
+
+
+def test_full_mask_4k_whole_tensors_match_the_oracle():
+    """The full-mask B=4 H=16 S=4096 D=128 workload at full size, in the launch
+    configuration the benchmark times: every element of dQ (after finalize),
+    dK and dV against the exact fp64 oracle (forward and backward over all 64
+    heads; O and LSE fed to the kernel are the oracle's, rounded as the
+    interface takes them), for shift and serialized ascending."""
+    w = WORKLOADS["full_b4_h16_s4096_d128"]
+    q, k, v, do = make_workload_inputs(w, seed=0)
+    workers = len(os.sched_getaffinity(0))
+    o_ex, lse_ex = A.attn_fwd(q, k, v, w.causal, row_block=2048, workers=workers)
+    dq_ref, dk_ref, dv_ref, _ = A.attn_bwd(q, k, v, o_ex, do, lse_ex, w.causal, row_block=2048, workers=workers)
+    dev = torch.device("cuda")
+    c = Case(w.B, w.Hq, w.Hkv, w.S, w.D, w.causal, q.to(dev), k.to(dev), v.to(dev),
+             torch.from_numpy(o_ex).to(torch.bfloat16).to(dev), do.to(dev),
+             torch.from_numpy(lse_ex).to(torch.float32).to(dev), None)
+    for sched in ("shift", "serialized_ascending"):
+        _, dqb, dk, dv = run_full(c, sched)
+        for name, got, ref in (("dq", dqb, dq_ref), ("dk", dk, dk_ref), ("dv", dv, dv_ref)):
+            rel, mx = err(got, ref)
+            assert rel <= REL_L2 and mx <= MAX_ABS, (sched, name, rel, mx)

@@ -336,6 +336,8 @@ int encode_2d(void* map_out, CUtensorMapDataType dt, int esize, const void* base
 }
 }  // namespace
 
+unsigned long long timeout_ns() { return g_timeout_ns.load(); }
+
 // bf16 [heads][S][D], boxes of 64 columns x 128 rows x 1 head (128 B rows,
 // swizzled).  Rows past S inside a head read as zero, so a ragged last tile
 // never touches the next head.  Strides S*D*2 and D*2 are multiples of 16.

@@ -181,6 +181,19 @@ int launch_group_sum(const float* part, void* out, int B, int Hkv, int G, int Sk
     return cudaGetLastError() == cudaSuccess ? 0 : -2;
 }
 
+// Loads (on the current device) the auxiliary kernels of the backward pass:
+// under lazy module loading a kernel's module is otherwise loaded at its first
+// launch.
+int load_aux_kernels() {
+    cudaFuncAttributes fa;
+    const void* fns[] = {(const void*)preprocess_kernel<64>, (const void*)preprocess_kernel<128>,
+                         (const void*)finalize_kernel, (const void*)finalize_tail_kernel,
+                         (const void*)task_start_kernel, (const void*)pair_time_kernel, (const void*)rank_kernel};
+    for (const void* f : fns)
+        if (cudaFuncGetAttributes(&fa, f) != cudaSuccess) return -2;
+    return 0;
+}
+
 int launch_build_ranks(int B, int Hq, int Hkv, int n, int causal, int sched, int P, uint16_t* ranks,
                        uint32_t* time, uint32_t* task_start, cudaStream_t st, int win, int nk) {
     const Shape s{B, Hq, Hkv, n, Hq / Hkv, causal, sched, win, nk};

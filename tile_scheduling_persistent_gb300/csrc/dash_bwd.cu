@@ -732,6 +732,18 @@ int launch_bwd_dispatch(int D, const BwdParams& prm, int grid, cudaStream_t stre
     return D == 64 ? launch_bwd<64, false, false>(prm, grid, stream) : launch_bwd<128, false, false>(prm, grid, stream);
 }
 
+// Loads (on the current device) every production variant of the persistent
+// kernel; under lazy module loading it would otherwise load at its first launch.
+int load_bwd_kernels() {
+    cudaFuncAttributes fa;
+    const void* fns[] = {(const void*)dash_bwd_kernel<64, false, false>, (const void*)dash_bwd_kernel<64, false, true>,
+                         (const void*)dash_bwd_kernel<128, false, false>,
+                         (const void*)dash_bwd_kernel<128, false, true>};
+    for (const void* f : fns)
+        if (cudaFuncGetAttributes(&fa, f) != cudaSuccess) return -2;
+    return 0;
+}
+
 int bwd_smem_bytes(int D) { return D == 64 ? Cfg<64>::kSmem : Cfg<128>::kSmem; }
 
 }  // namespace dash

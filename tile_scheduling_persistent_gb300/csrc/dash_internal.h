@@ -11,6 +11,7 @@ struct BwdParams;
 int launch_bwd_dispatch(int D, const BwdParams& prm, int grid, cudaStream_t stream);
 int bwd_max_ctas(int D, int device, int* P);
 int bwd_smem_bytes(int D);
+int load_bwd_kernels();   // load every production variant on the current device
 
 // Auxiliary kernels (dash_aux.cu).
 int launch_preprocess(const void* o, const void* dO, float* delta, long long rows, int D, cudaStream_t s);
@@ -18,6 +19,7 @@ int launch_finalize(const float* src, void* dst, size_t numel, cudaStream_t s);
 // dK / dV of a backward run with one task per query head: out bf16
 // [B, Hkv, Skv, D] = the fp32 part [B, Hkv*G, Skv, D] summed over each group
 // of G query heads in ascending order.
+int load_aux_kernels();   // load the auxiliary backward kernels on the current device
 int launch_group_sum(const float* part, void* out, int B, int Hkv, int G, int Skv, int D, cudaStream_t s);
 // Accumulation ranks of a static schedule, built on the device:
 // ranks [B*Hq*n][n] (uint16), scratch `time` [B*Hq*n][n] (uint32),
@@ -35,6 +37,9 @@ int launch_fwd(const void* q, const void* k, const void* v, void* o, float* lse,
 int run_tile_probe(const void* k, const void* v, const void* q, const void* dO, const float* lse,
                    const float* delta, int D, int diag, float* sT, float* pT, float* dpT, float* dsT,
                    float* dv, float* dk, float* dq);
+
+// Timeout of every device-side wait, in ns, as dash_set_timeout_ns set it (dash_api.cu).
+unsigned long long timeout_ns();
 
 // Tensor maps (dash_api.cu).
 int make_tmap_2d(void* map_out, const void* base, long long rows, int D);

@@ -16,6 +16,13 @@
 // must start at zero is cleared on the stream at the start of each call, and
 // two calls whose executions overlap on the GPU (different streams, or
 // different host threads) race on the array.
+//
+// Set-up, once per device: dash_noalloc_init (or else the first call) looks
+// up the device address of g_scratch with that device current and loads the
+// backward kernels.  Under lazy module loading that is when the driver loads
+// the library's module and reserves the array's memory, so it belongs before
+// a caller's pool takes the device and before its latency-critical path or
+// any stream capture.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -38,21 +45,43 @@ constexpr int kMaxDevices = 64;
 std::mutex g_setup_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of g_scratch on `dev` (the current device); looked up once
-// per device.  In host code the symbol is only a host-side stand-in.
+// Looks up the device address of g_scratch on `dev` (the current device) and
+// loads the kernels this entry point launches.  In host code the symbol is
+// only a host-side stand-in; the kernels get the looked-up address.
+int setup_device(int dev) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) {
+        (void)cudaGetLastError();
+        return DASH_ERR_CUDA;
+    }
+    int P = 0;
+    if (bwd_max_ctas(64, dev, &P) || bwd_max_ctas(128, dev, &P) || load_bwd_kernels() || load_aux_kernels()) {
+        (void)cudaGetLastError();
+        return DASH_ERR_CUDA;
+    }
+    g_scratch_ptr[dev] = p;
+    return DASH_OK;
+}
+
+// Device address of g_scratch on `dev`, set up on first use.
 int scratch_for_device(int dev, unsigned char** out) {
     if (dev < 0 || dev >= kMaxDevices) return DASH_ERR_DEVICE;
     std::lock_guard<std::mutex> lk(g_setup_mu);
     if (!g_scratch_ptr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) {
-            (void)cudaGetLastError();
-            return DASH_ERR_CUDA;
-        }
-        g_scratch_ptr[dev] = p;
+        const int rc = setup_device(dev);
+        if (rc) return rc;
     }
     *out = static_cast<unsigned char*>(g_scratch_ptr[dev]);
     return DASH_OK;
+}
+
+int current_sm103(int* dev) {
+    int major = 0, minor = 0;
+    if (cudaGetDevice(dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, *dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, *dev) != cudaSuccess)
+        return DASH_ERR_CUDA;
+    return (major == 10 && minor == 3) ? DASH_OK : DASH_ERR_DEVICE;
 }
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
@@ -75,14 +104,11 @@ extern "C" int dash_attn_bwd_noalloc(const dash_bf16* q, const dash_bf16* k, con
         (S + 127) / 128 > 65535)
         return DASH_ERR_ARG;
     if (schedule == kAuto) schedule = select_schedule(D, causal);
-    int dev = 0, major = 0, minor = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-        return DASH_ERR_CUDA;
-    if (major != 10 || minor != 3) return DASH_ERR_DEVICE;
+    int dev = 0;
+    int rc = current_sm103(&dev);
+    if (rc) return rc;
     int P = 0;
-    int rc = bwd_max_ctas(D, dev, &P);
+    rc = bwd_max_ctas(D, dev, &P);
     if (rc == -3) return DASH_ERR_LAUNCH;
     if (rc) return DASH_ERR_CUDA;
 
@@ -134,7 +160,7 @@ extern "C" int dash_attn_bwd_noalloc(const dash_bf16* q, const dash_bf16* k, con
     prm.abort_flag = ints + 9;
     prm.sem = ints + 16;
     prm.logcnt = ints + 16 + kSubTiles * tiles;
-    prm.timeout_ns = 2000000000ull;
+    prm.timeout_ns = timeout_ns();   // as dash_set_timeout_ns set it
     prm.ntasks = ntasks;
     prm.B = B;
     prm.Hq = Hq;
@@ -154,4 +180,29 @@ extern "C" int dash_attn_bwd_noalloc(const dash_bf16* q, const dash_bf16* k, con
     rc = launch_bwd_dispatch(D, prm, P, stream);
     if (rc == -3) return DASH_ERR_LAUNCH;
     return rc ? DASH_ERR_CUDA : DASH_OK;
+}
+
+extern "C" int dash_noalloc_init(void) {
+    int dev = 0;
+    int rc = current_sm103(&dev);
+    if (rc) return rc;
+    if (dev >= kMaxDevices) return DASH_ERR_DEVICE;
+    std::lock_guard<std::mutex> lk(g_setup_mu);
+    return setup_device(dev);
+}
+
+extern "C" int dash_get_status_noalloc(dash_stream_t stream, int* code, int* info) {
+    if (!code) return DASH_ERR_ARG;
+    int dev = 0;
+    int rc = current_sm103(&dev);
+    if (rc) return rc;
+    unsigned char* base = nullptr;
+    if ((rc = scratch_for_device(dev, &base))) return rc;
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return DASH_ERR_CUDA;
+    int h[8] = {0};
+    if (cudaMemcpy(h, base, sizeof(h), cudaMemcpyDeviceToHost) != cudaSuccess) return DASH_ERR_CUDA;
+    *code = h[0];
+    if (info)
+        for (int i = 0; i < 4; ++i) info[i] = h[1 + i];
+    return DASH_OK;
 }

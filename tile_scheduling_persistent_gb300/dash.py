@@ -28,6 +28,7 @@ EXPORTS = (
     "dash_attn_bwd_debug", "dash_debug_tile_probe", "dash_attn_bwd_noalloc", "dash_select_schedule",
     "dash_attn_fwd", "dash_sim_schedule_band", "dash_attn_bwd_window", "dash_attn_fwd_window",
     "dash_sim_schedule_cross", "dash_attn_bwd_cross", "dash_attn_fwd_cross", "dash_head_split",
+    "dash_noalloc_init", "dash_get_status_noalloc",
 )
 
 
@@ -64,6 +65,8 @@ def lib():
     L.dash_attn_bwd_noalloc.argtypes = [P] * 9 + [I] * 7 + [P]
     L.dash_dq_finalize.argtypes = [P, P, Z, P]
     L.dash_get_status.argtypes = [P, ctypes.POINTER(I), ctypes.POINTER(I)]
+    L.dash_get_status_noalloc.argtypes = [P, ctypes.POINTER(I), ctypes.POINTER(I)]
+    L.dash_noalloc_init.argtypes = []
     L.dash_set_timeout_ns.argtypes = [ctypes.c_uint64]
     L.dash_release_workspaces.argtypes = []
     L.dash_num_ctas.argtypes = [I, ctypes.POINTER(I)]
@@ -143,6 +146,19 @@ def attn_bwd_noalloc(q, k, v, o, do, lse, dq, dk, dv, causal, schedule, stream=N
     fixed device array (see dash_attn_bwd_noalloc in include/dash.h)."""
     _check(lib().dash_attn_bwd_noalloc(*_bwd_args(q, k, v, o, do, lse, dq, dk, dv, causal, schedule),
                                        _stream(stream)), "dash_attn_bwd_noalloc")
+
+
+def noalloc_init():
+    """Set-up of attn_bwd_noalloc on the current device (scratch address, kernels loaded)."""
+    _check(lib().dash_noalloc_init(), "dash_noalloc_init")
+
+
+def get_status_noalloc(stream=None):
+    """(code, info) of the last attn_bwd_noalloc on the current device; synchronizes `stream`."""
+    code = ctypes.c_int(0)
+    info = (ctypes.c_int * 4)()
+    _check(lib().dash_get_status_noalloc(_stream(stream), ctypes.byref(code), info), "dash_get_status_noalloc")
+    return code.value, list(info)
 
 
 def attn_bwd_debug(q, k, v, o, do, lse, dq, dk, dv, causal, schedule, stream=None, order_log=None,
