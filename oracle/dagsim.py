@@ -179,6 +179,15 @@ def make_tasks(schedule: str, B: int, Hq: int, Hkv: int, n: int, causal: bool, b
         # head group k % (B*Hkv), so that each wave holds tiles of similar length
         groups = B * Hkv
         tasks = [tasks[g * n + j] for j in range(n) for g in range(groups)]
+    elif schedule in STATIC and band is None and nkv is None and (not causal or schedule == "symmetric_shift"):
+        # shift on a full mask and symmetric shift (full or causal) are dealt by
+        # the parity of the task's tile (pair) index: the even tiles of every
+        # head group first, then the odd ones.  Within a wave a dQ tile then
+        # receives a contribution every second step of the rotation instead of
+        # every step, while the task -> worker rule stays k -> k mod P.
+        groups = B * Hkv
+        T = len(tasks) // groups
+        tasks = [tasks[g * T + t] for par in range(2) for g in range(groups) for t in range(par, T, 2)]
     return tasks
 
 

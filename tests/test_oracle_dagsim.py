@@ -68,11 +68,17 @@ def test_rotation_lists_n4():
     for line in golden_rows("shift_rotation_n4.txt"):
         sm, tiles = line.split(":")
         want[int(sm)] = [int(t) for t in tiles.split()]
+    # the worker that owns KV tile j visits row j of the figure (whichever of
+    # the P workers the dealing gives that tile to)
     s = G.build("shift", 1, 1, 1, 4, False, 4)
+    seen = set()
     for cta in range(4):
         (k,) = s.cta_tasks[cta]
-        assert [p.i for p in s.tasks[k]] == want[cta]
-        assert all(p.j == cta for p in s.tasks[k])
+        j = s.tasks[k][0].j
+        assert all(p.j == j for p in s.tasks[k])
+        assert [p.i for p in s.tasks[k]] == want[j]
+        seen.add(j)
+    assert seen == {0, 1, 2, 3}
 
 
 def no_waits(s, c, r):
@@ -248,3 +254,30 @@ def test_band_wide_enough_is_causal():
             continue   # with a band it is read as shift
         assert a.tasks == b.tasks
         assert a.turn == b.turn
+
+
+@pytest.mark.parametrize("schedule,causal,n", [("shift", False, 8), ("symmetric_shift", True, 16),
+                                               ("symmetric_shift", False, 6)])
+def test_parity_dealing_spaces_a_tiles_contributions_two_steps_apart(schedule, causal, n):
+    # Full-mask shift and symmetric shift deal the even tiles (pairs) of every
+    # head group first, then the odd ones; with one wave per parity class, the
+    # contributions a dQ tile receives from one wave are at least two steps of
+    # the rotation apart (head-major dealing would give one every step).
+    B, H = 1, 4
+    s = G.build(schedule, B, H, H, n, causal, P=10 ** 6)
+    T = len(s.tasks) // (B * H)
+    even = (T + 1) // 2
+    for k, t in enumerate(s.tasks):
+        parity = 0 if k < B * H * even else 1
+        tiles = {p.j for p in t}
+        if schedule == "shift":
+            assert tiles == {(k % even) * 2 + parity if parity == 0 else ((k - B * H * even) % (T // 2)) * 2 + 1}
+    for par in range(2):
+        wave = [k for k in range(len(s.tasks)) if (k < B * H * even) == (par == 0)]
+        times = {}
+        for k in wave:
+            for step, p in enumerate(s.tasks[k]):
+                times.setdefault((p.b, p.hq, p.i), []).append(step)
+        for tile, ts in times.items():
+            ts.sort()
+            assert all(b - a >= 2 for a, b in zip(ts, ts[1:])), (schedule, tile, ts)

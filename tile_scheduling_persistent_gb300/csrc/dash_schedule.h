@@ -87,14 +87,24 @@ DASH_HD int kv_len(const Shape& s, int j) {
 // whose accumulation order is ascending KV).
 DASH_HD int first_kv(const Shape& s, int q) { return (s.causal && s.win && q >= s.win) ? q - s.win + 1 : 0; }
 
-// Task numbering.  Head-group-major (task k = tile k % T of group k / T)
-// except causal shift without a window, which is KV-tile-major (tile
-// k / (B*Hkv) of group k % (B*Hkv)): a causal KV tile j has n - j pairs, and
-// dealing the tasks round-robin in that order gives every wave tiles of
-// nearly equal length (busiest of 152 workers at 1.035x the mean instead of
-// 1.09x for B1 H32 S16384) and spaces the contributions to a dQ tile about a
-// wave apart.
+// Task numbering (the dealing rule is task k -> worker k mod P throughout).
+//  - Causal shift without a window is KV-tile-major (tile k / (B*Hkv) of group
+//    k % (B*Hkv)): a causal KV tile j has n - j pairs, and dealing the tasks
+//    round-robin in that order gives every wave tiles of nearly equal length
+//    (busiest of 152 workers at 1.035x the mean instead of 1.09x for B1 H32
+//    S16384) and spaces the contributions to a dQ tile about a wave apart.
+//  - Shift on a full mask and symmetric shift (full or causal), with equal
+//    query and key lengths and no window, are parity-major: the even tiles
+//    (pairs) of every head group, head group by head group, then the odd
+//    ones.  All of a head's tiles in one wave would add into each of its dQ
+//    tiles at every step of the rotation; a wave of one parity adds at every
+//    second step, which leaves each ordered link two steps to complete.
+//  - Everything else is head-group-major (tile k % T of group k / T).
 DASH_HD bool kv_major(const Shape& s) { return s.sched == kShift && s.causal && !s.win; }
+DASH_HD bool parity_major(const Shape& s) {
+    return !s.win && !s.nk && (s.sched == kShift || s.sched == kSymmetric) &&
+           (!s.causal || s.sched == kSymmetric);
+}
 
 // A task's tile (or symmetric pair) and head group (b * Hkv + hkv); callers
 // that walk a task's pairs compute it once per task.  Task counts are below
@@ -109,6 +119,17 @@ DASH_HD TaskRef task_ref(const Shape& s, int64_t k) {
         const int g = s.B * s.Hkv;
         r.t = kk / g;
         r.bh = kk - r.t * g;
+    } else if (parity_major(s)) {
+        const int g = s.B * s.Hkv, T = tasks_per_group(s);
+        const int even = (T + 1) / 2;   // even tiles per group, then T / 2 odd ones
+        if (kk < g * even) {
+            r.bh = kk / even;
+            r.t = 2 * (kk - r.bh * even);
+        } else {
+            const int x = kk - g * even, odd = T / 2;
+            r.bh = x / odd;
+            r.t = 2 * (x - r.bh * odd) + 1;
+        }
     } else {
         const int T = tasks_per_group(s);
         r.bh = kk / T;
