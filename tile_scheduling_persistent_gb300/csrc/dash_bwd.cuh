@@ -145,12 +145,16 @@ struct Cfg {
 
 // Register split of the five warpgroups (setmaxnreg); the launch must grant
 // kRegsLaunch registers per thread so that the split fits the block's pool.
+// At D = 128 the producer / MMA warpgroup gets 80: at 64 its spilled values
+// are reloaded through the load/store path that the drain warps' reductions
+// keep busy, which delays every MMA issue (measured: 8% on the unordered
+// kernel); the softmax warps give up the 8 registers.
 constexpr int kRegsLaunch = 96;
 template <int D>
 struct Regs {
-    static constexpr int kCtl = 64;
+    static constexpr int kCtl = (D == 128) ? 80 : 64;
     static constexpr int kDrain = (D == 128) ? 96 : 80;
-    static constexpr int kSoftmax = (D == 128) ? 112 : 120;
+    static constexpr int kSoftmax = (D == 128) ? 104 : 120;
     static_assert(128 * kCtl + 256 * kDrain + 256 * kSoftmax <= kThreads * kRegsLaunch, "register split");
 };
 
