@@ -355,31 +355,19 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                         trace_ev<kProf>(p, pp + 1, EV_S_ISSUE);
                     }
                     if (!wait1(BAR(B_DS_READY), (uint32_t)(pp & 1), c, kRoleMma, (int)pp, 7)) break;
-                    if constexpr (!C::kDqAlias) {
-                        // dQ has columns of its own: issue it before dK, so that the
-                        // drain warps get it one product earlier
-                        if (pp > 0 && !wait1(BAR(B_DQ_EMPTY), (uint32_t)((pp - 1) & 1), c, kRoleMma, (int)pp, 8))
-                            break;
-                        ptx::tc_fence_after();
-                        issue_dq<D>(tDQ, sDS, sK);
-                        ptx::tc_commit(BAR(B_DQ_FULL));
-                        trace_ev<kProf>(p, pp, EV_DQ_ISSUE);
-                        issue_dk<D>(tDK, sDS, sQ(pp), kv_first ? 0u : 1u);
-                        ptx::tc_commit(BAR(B_Q_EMPTY + (int)(pp % C::kQStages)));
-                        trace_ev<kProf>(p, pp, EV_DK_ISSUE);
-                        ptx::tc_commit(BAR(B_DS_FREE));
-                    } else {
-                        // dQ reuses the dP columns, which dS has just freed; dK first
-                        ptx::tc_fence_after();
-                        issue_dk<D>(tDK, sDS, sQ(pp), kv_first ? 0u : 1u);
-                        ptx::tc_commit(BAR(B_Q_EMPTY + (int)(pp % C::kQStages)));
-                        trace_ev<kProf>(p, pp, EV_DK_ISSUE);
-                        ptx::tc_fence_after();
-                        issue_dq<D>(tDQ, sDS, sK);
-                        trace_ev<kProf>(p, pp, EV_DQ_ISSUE);
-                        ptx::tc_commit(BAR(B_DS_FREE));
-                        ptx::tc_commit(BAR(B_DQ_FULL));
-                    }
+                    // dQ is issued before dK, so that the drain warps get it one product
+                    // earlier (at D = 128 it reuses the dP columns, which dS has just freed)
+                    if (!C::kDqAlias && pp > 0 &&
+                        !wait1(BAR(B_DQ_EMPTY), (uint32_t)((pp - 1) & 1), c, kRoleMma, (int)pp, 8))
+                        break;
+                    ptx::tc_fence_after();
+                    issue_dq<D>(tDQ, sDS, sK);
+                    ptx::tc_commit(BAR(B_DQ_FULL));
+                    trace_ev<kProf>(p, pp, EV_DQ_ISSUE);
+                    issue_dk<D>(tDK, sDS, sQ(pp), kv_first ? 0u : 1u);
+                    ptx::tc_commit(BAR(B_Q_EMPTY + (int)(pp % C::kQStages)));
+                    trace_ev<kProf>(p, pp, EV_DK_ISSUE);
+                    ptx::tc_commit(BAR(B_DS_FREE));
                     if (d.flags & kKvLast) {
                         ptx::tc_commit(BAR(B_ACC_FULL));
                         ptx::tc_commit(BAR(B_KV_EMPTY));

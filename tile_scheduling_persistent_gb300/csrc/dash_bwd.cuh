@@ -42,7 +42,8 @@
 //
 // Tensor memory (512 columns): dK [0,D), dV [D,2D), S/P [2D, 2D+128),
 // dP [2D+128, 2D+256); dQ aliases dP when D = 128 and has its own 64
-// columns when D = 64.
+// columns when D = 64.  dQ is issued before dK, so the drain warps get it
+// one product earlier.
 //
 // Every wait is bounded (%globaltimer); a wait that runs out records the
 // failure in the status word, raises a CTA-wide and a grid-wide abort flag,
