@@ -18,6 +18,8 @@ struct Ctl {
     int* abort_global;
     unsigned long long timeout;
     unsigned long long* prof;   // per-CTA cycle counters in shared memory, or null
+    uint32_t suspend_ns;        // mbarrier waits: suspend-time hint (0 = plain polls)
+    int poll_ns;                // accumulation-turn polls: sleep between two reads
 };
 
 // Cycle counters (debug): slot = role * kProfPerRole + site.  One thread per
@@ -51,7 +53,7 @@ __device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, const Ctl& 
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const unsigned long long c0 = clock64();
     const uint64_t t0 = ptx::globaltimer();
-    while (!ptx::mbar_try_wait(bar, parity)) {
+    while (!(c.suspend_ns ? ptx::mbar_try_wait_hint(bar, parity, c.suspend_ns) : ptx::mbar_try_wait(bar, parity))) {
         if (*c.abort_smem) return false;
         if (ptx::globaltimer() - t0 > c.timeout) {
             report_timeout(c, role, i0, site, (int)bar);
@@ -99,7 +101,7 @@ __device__ bool wait_turn(const BwdParams& p, const Ctl& c, volatile int* abort_
                 return false;
             }
         }
-        __nanosleep(32);
+        __nanosleep(c.poll_ns);
     }
 }
 
@@ -126,7 +128,12 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
 
     constexpr bool prof_on = kProf;   // cycle counters compiled in only for the debug instantiation
     const bool prof_rec = prof_on && lane == 0 && (warp == 0 || warp == 1 || warp == 4 || warp == 8);
-    const Ctl c{abort_smem, p.status, p.abort_flag, p.timeout_ns, prof_rec ? prof_smem : nullptr};
+    // At D = 128 waiting warps sleep in their mbarrier waits (1 us hint) and
+    // poll the accumulation turn every 256 ns, leaving issue slots and the
+    // load/store path to the working warps (+4% deterministic on the full
+    // S = 4096 workload); at D = 64 the plain polls measured faster.
+    const Ctl c{abort_smem, p.status, p.abort_flag, p.timeout_ns, prof_rec ? prof_smem : nullptr,
+                D == 128 ? 1000u : 0u, D == 128 ? 256 : 32};
     const unsigned long long t_start = kProf ? clock64() : 0ull;
     const uint32_t sbase = ptx::smem_u32(smem);
 
@@ -542,6 +549,9 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+                // the barrier orders the other lanes' reductions after lane 0's
+                // acquire (a shuffle alone carries no memory ordering)
+                __syncwarp();
             } else if (st == 0 && p.order_log && lane == 0) {
                 const int s = atomicAdd(p.logcnt + tile, 1);
                 if (s >= 0 && s < p.nkv) p.order_log[(size_t)tile * p.nkv + s] = d.kv;
@@ -589,7 +599,8 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
 #pragma unroll
                     for (int cc = 0; cc < D / 32; ++cc) {
                         uint32_t v[32];
-                        ptx::tmem_ld32(tmem + kv_lanes + col + 32 * cc, v);
+                        ptx::tmem_ld16(tmem + kv_lanes + col + 32 * cc, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                        ptx::tmem_ld16(tmem + kv_lanes + col + 32 * cc + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
                         ptx::tmem_ld_wait();
                         if (!krow_ok) continue;
                         if (f32) {
@@ -617,7 +628,8 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
 #pragma unroll
                     for (int cc = 0; cc < D / 32; ++cc) {
                         uint32_t v[32];
-                        ptx::tmem_ld32(tmem + kv_lanes + col + 32 * cc, v);
+                        ptx::tmem_ld16(tmem + kv_lanes + col + 32 * cc, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                        ptx::tmem_ld16(tmem + kv_lanes + col + 32 * cc + 16, *reinterpret_cast<uint32_t(*)[16]>(&v[16]));
                         ptx::tmem_ld_wait();
                         uint32_t pk[16];
 #pragma unroll
