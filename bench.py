@@ -38,7 +38,12 @@ METRIC = "deterministic attn-bwd TFLOP/s & % of BF16 peak; det/nondet throughput
 # schedule), each from one ncu capture, with the SHA-256 (first 16 hex digits)
 # of the kernel source it was taken on.  A figure is reported only while the
 # kernel source still has that hash; otherwise the roofline's traffic is null.
-NCU_TRAFFIC = {}
+NCU_TRAFFIC = {
+    ("full_b4_h16_s4096_d128", "shift"): (1060397568, "2c961505dc1ebff0"),
+    ("causal_b4_h16_s8192_d128", "symmetric_shift"): (2328263168, "2c961505dc1ebff0"),
+    ("causal_b1_h32_s16384_d64", "shift"): (7089124096, "2c961505dc1ebff0"),
+    ("gqa_causal_b1_hq32_hkv8_s16384_d128", "symmetric_shift"): (2703636992, "2c961505dc1ebff0"),
+}
 KERNEL_SOURCES = ("tile_scheduling_persistent_gb300/csrc/dash_bwd.cu",
                   "tile_scheduling_persistent_gb300/csrc/dash_bwd.cuh",
                   "tile_scheduling_persistent_gb300/csrc/dash_ptx.cuh",
