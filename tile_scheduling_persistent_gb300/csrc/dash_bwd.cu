@@ -66,7 +66,12 @@ __device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, const Ctl& 
 
 // Whole-warp bounded wait with a warp-uniform outcome: lane 0 polls, then
 // every lane observes the completed phase itself (acquire per thread).
+// kFast: first one try_wait by every lane and a vote, which returns at once
+// when the phase has already completed (one shared-memory round trip instead
+// of three); the polled path only when it has not.
+template <bool kFast = false>
 __device__ __forceinline__ bool waitw(uint32_t bar, uint32_t parity, const Ctl& c, int role, int i0, int site) {
+    if (kFast && __all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
     int ok = 1;
     if ((threadIdx.x & 31) == 0) ok = wait1(bar, parity, c, role, i0, site) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -415,21 +420,55 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
         const uint32_t lane_off = (uint32_t)(32 * sub) << 16;
         uint8_t* ds_box = smem + C::OFF_DS + (c0 >> 6) * kBox;
         const bool rec = warp == 8 && lane == 0;
-        for (long long pp = 0;; ++pp) {
-            const int ds = (int)(pp % kNDesc);
-            if (!waitw(BAR(B_DESC_FULL + ds), (uint32_t)((pp / kNDesc) & 1), c, kRoleSoftmax, (int)pp, 0)) break;
-            const PairDesc d = descs[ds];
-            if (d.flags & kEnd) break;
-            // per-column statistics of this pair's Q tile: lane l holds columns c0+l and c0+32+l
-            // (columns past S of a partial last tile read 0 and are masked)
-            const int qcol = d.q * 128 + c0 + lane;
-            const size_t qrow = (size_t)(d.b * p.Hq + d.hq) * p.S + (size_t)qcol;
+        // Per-column statistics of a pair's Q tile: lane l holds LSE and delta
+        // of columns c0+l and c0+32+l (columns past S of a partial last tile
+        // read 0 and are masked).
+        // sv: LSE of the two columns (times log2(e) at D = 64, where the
+        // values are used at once), then their delta.
+        constexpr bool kAhead = (D == 128);
+        constexpr float kLseMul = kAhead ? 1.f : kLog2e;
+        auto fetch = [&](const PairDesc& fd, float (&sv)[4]) {
+            const int qcol = fd.q * 128 + c0 + lane;
+            const size_t qrow = (size_t)(fd.b * p.Hq + fd.hq) * p.S + (size_t)qcol;
             const bool va = !kMasked || qcol < p.S, vb = !kMasked || qcol + 32 < p.S;
-            const float lse2_a = va ? ptx::ld_nc(p.lse + qrow) * kLog2e : 0.f;
-            const float lse2_b = vb ? ptx::ld_nc(p.lse + qrow + 32) * kLog2e : 0.f;
-            const float delta_a = va ? ptx::ld_nc(p.delta + qrow) : 0.f;
-            const float delta_b = vb ? ptx::ld_nc(p.delta + qrow + 32) : 0.f;
-            if (!waitw(BAR(B_S_FULL), (uint32_t)(pp & 1), c, kRoleSoftmax, (int)pp, 1)) break;
+            sv[0] = va ? ptx::ld_nc(p.lse + qrow) * kLseMul : 0.f;
+            sv[1] = vb ? ptx::ld_nc(p.lse + qrow + 32) * kLseMul : 0.f;
+            sv[2] = va ? ptx::ld_nc(p.delta + qrow) : 0.f;
+            sv[3] = vb ? ptx::ld_nc(p.delta + qrow + 32) : 0.f;
+        };
+        // At D = 128 the next pair's descriptor is read at the top of this
+        // pair and its statistics are loaded after this pair's P phase, so
+        // that the shared-memory read and the global loads overlap the dP wait
+        // and the dS phase; at D = 64 (measured faster there) a pair's
+        // descriptor and statistics are read at the top of its own iteration.
+        PairDesc d{};
+        float sv[4] = {0.f, 0.f, 0.f, 0.f};
+        if constexpr (kAhead) {
+            if (waitw<true>(BAR(B_DESC_FULL), 0u, c, kRoleSoftmax, 0, 0)) {
+                d = descs[0];
+                if (!(d.flags & kEnd)) fetch(d, sv);
+            } else {
+                d.flags = kEnd;
+            }
+        }
+        for (long long pp = 0;; ++pp) {
+            PairDesc nd;
+            if constexpr (kAhead) {
+                if (d.flags & kEnd) break;
+                const int ns = (int)((pp + 1) % kNDesc);
+                if (!waitw<true>(BAR(B_DESC_FULL + ns), (uint32_t)(((pp + 1) / kNDesc) & 1), c, kRoleSoftmax, (int)pp, 0))
+                    break;
+                nd = descs[ns];
+            } else {
+                const int ds = (int)(pp % kNDesc);
+                if (!waitw<true>(BAR(B_DESC_FULL + ds), (uint32_t)((pp / kNDesc) & 1), c, kRoleSoftmax, (int)pp, 0)) break;
+                d = descs[ds];
+                if (d.flags & kEnd) break;
+                fetch(d, sv);
+            }
+            const float lse2_a = kAhead ? sv[0] * kLog2e : sv[0], lse2_b = kAhead ? sv[1] * kLog2e : sv[1];
+            const float delta_a = sv[2], delta_b = sv[3];
+            if (!waitw<true>(BAR(B_S_FULL), (uint32_t)(pp & 1), c, kRoleSoftmax, (int)pp, 1)) break;
             if (rec) trace_ev<kProf>(p, pp, EV_SM_S_SEEN);
             ptx::tc_fence_after();
             float P[64];
@@ -442,10 +481,12 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(BAR(B_P_READY));
             if (rec) trace_ev<kProf>(p, pp, EV_SM_P_DONE);
-            if (!waitw(BAR(B_DP_FULL), (uint32_t)(pp & 1), c, kRoleSoftmax, (int)pp, 2)) break;
+            float svn[4] = {0.f, 0.f, 0.f, 0.f};
+            if (kAhead && !(nd.flags & kEnd)) fetch(nd, svn);
+            if (!waitw<true>(BAR(B_DP_FULL), (uint32_t)(pp & 1), c, kRoleSoftmax, (int)pp, 2)) break;
             if (rec) trace_ev<kProf>(p, pp, EV_SM_DP_SEEN);
             ptx::tc_fence_after();
-            if (pp > 0 && !waitw(BAR(B_DS_FREE), (uint32_t)((pp - 1) & 1), c, kRoleSoftmax, (int)pp, 3)) break;
+            if (pp > 0 && !waitw<true>(BAR(B_DS_FREE), (uint32_t)((pp - 1) & 1), c, kRoleSoftmax, (int)pp, 3)) break;
             tc0 = kProf ? clock64() : 0ull;
             ds_64(tmem + lane_off + C::COL_DP, c0, delta_a, delta_b, p.scale, P, ds_box, row);
             prof_add(c, kRoleSoftmax, 9, tc0);
@@ -454,10 +495,18 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(BAR(B_DS_READY));
             if (rec) trace_ev<kProf>(p, pp, EV_SM_DS_DONE);
+            if constexpr (kAhead) {
+                d = nd;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) sv[k] = svn[k];
+            }
         }
     } else {
         if constexpr (Regs<D>::kDrain < kRegsLaunch) ptx::setmaxnreg_dec<Regs<D>::kDrain>();   // 96 at D = 128: as launched
         // ================================================== dQ drain + ordered reduction + dK/dV epilogue
+        // Fast-path waits here only at D = 64: at D = 128 a drain that reaches
+        // its turn sooner lengthens the ordered chain (measured 5-9% slower).
+        constexpr bool kDrainFast = (D == 64);
         const int sub = warp & 3;
         const int half = (wg == 4) ? 1 : 0;
         const int st = 2 * sub + half;                     // dQ sub-tile: rows 16*st .. 16*st+15
@@ -470,10 +519,10 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
         int kvc = 0;
         for (long long pp = 0;; ++pp) {
             const int ds = (int)(pp % kNDesc);
-            if (!waitw(BAR(B_DESC_FULL + ds), (uint32_t)((pp / kNDesc) & 1), c, kRoleDrain, (int)pp, 0)) break;
+            if (!waitw<kDrainFast>(BAR(B_DESC_FULL + ds), (uint32_t)((pp / kNDesc) & 1), c, kRoleDrain, (int)pp, 0)) break;
             const PairDesc d = descs[ds];
             if (d.flags & kEnd) break;
-            if (!waitw(BAR(B_DQ_FULL), (uint32_t)(pp & 1), c, kRoleDrain, (int)pp, 1)) break;
+            if (!waitw<kDrainFast>(BAR(B_DQ_FULL), (uint32_t)(pp & 1), c, kRoleDrain, (int)pp, 1)) break;
             if (rec) trace_ev<kProf>(p, pp, EV_DR_DQ_SEEN);
             ptx::tc_fence_after();
             // Read the sub-tile (16 rows x D) out of tensor memory, then hand the
@@ -583,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
             if (lane == 0) ptx::mbar_arrive(BAR(B_DESC_EMPTY + ds));
             if (d.flags & kKvLast) {
                 // dK (drain warps of WG1) and dV (WG4) of the finished KV tile
-                if (!waitw(BAR(B_ACC_FULL), (uint32_t)(kvc & 1), c, kRoleDrain, (int)pp, 2)) break;
+                if (!waitw<kDrainFast>(BAR(B_ACC_FULL), (uint32_t)(kvc & 1), c, kRoleDrain, (int)pp, 2)) break;
                 ptx::tc_fence_after();
                 const int krow = 32 * sub + lane;
                 const bool krow_ok = !kMasked || d.kv * 128 + krow < p.Skv;   // rows past S_kv are not stored
