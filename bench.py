@@ -247,7 +247,10 @@ def time_schedule(w, sched, tensors, outs, steps, warmup, stream, kernel_events=
     code, info = dash.get_status(stream)
     if code != 0:
         raise RuntimeError("device status %d %s" % (code, info))
-    return ms, kms, 3   # preprocess + persistent kernel + finalize
+    # preprocess + persistent kernel + finalize, and the two group sums (dK,
+    # dV) when the shape runs one task per query head
+    split = dash.head_split(sched, w.causal, w.B, w.Hq, w.Hkv, w.S, w.D, dash.num_ctas(), w.window, w.Skv)
+    return ms, kms, 3 + (2 if split else 0)
 
 
 class Ranks:
