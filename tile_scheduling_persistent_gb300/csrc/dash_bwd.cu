@@ -452,7 +452,7 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
             }
         }
         for (long long pp = 0;; ++pp) {
-            PairDesc nd;
+            PairDesc nd{};
             if constexpr (kAhead) {
                 if (d.flags & kEnd) break;
                 const int ns = (int)((pp + 1) % kNDesc);
