@@ -39,10 +39,10 @@ METRIC = "deterministic attn-bwd TFLOP/s & % of BF16 peak; det/nondet throughput
 # of the kernel source it was taken on.  A figure is reported only while the
 # kernel source still has that hash; otherwise the roofline's traffic is null.
 NCU_TRAFFIC = {
-    ("full_b4_h16_s4096_d128", "shift"): (689012992 + 368568576, "068b2048590b0cc7"),
-    ("causal_b4_h16_s8192_d128", "symmetric_shift"): (1473325312 + 854506496, "068b2048590b0cc7"),
-    ("causal_b1_h32_s16384_d64", "shift"): (3777728768 + 1931084544, "068b2048590b0cc7"),
-    ("gqa_causal_b1_hq32_hkv8_s16384_d128", "symmetric_shift"): (1429903872 + 1210017792, "068b2048590b0cc7"),
+    ("full_b4_h16_s4096_d128", "shift"): (687228160 + 362156800, "baadc158122b17ae"),
+    ("causal_b4_h16_s8192_d128", "symmetric_shift"): (1472157696 + 846804480, "baadc158122b17ae"),
+    ("causal_b1_h32_s16384_d64", "shift"): (3742285312 + 1901929728, "baadc158122b17ae"),
+    ("gqa_causal_b1_hq32_hkv8_s16384_d128", "symmetric_shift"): (1432983552 + 1193677824, "baadc158122b17ae"),
 }
 KERNEL_SOURCES = ("tile_scheduling_persistent_gb300/csrc/dash_bwd.cu",
                   "tile_scheduling_persistent_gb300/csrc/dash_bwd.cuh",
