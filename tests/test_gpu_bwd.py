@@ -206,8 +206,9 @@ def test_finalize_round_to_nearest_even():
     assert torch.equal(dst.cpu().view(torch.int16), want.view(torch.int16))
 
 
-def test_missing_predecessor_times_out_and_context_survives():
-    c = case("causal_s512_d64")
+@pytest.mark.parametrize("name", ["causal_s512_d64", "causal_s1024_d128"])
+def test_missing_predecessor_times_out_and_context_survives(name):
+    c = case(name)
     P = dash.num_ctas()
     _, turns, _ = dash.sim_schedule("shift", c.causal, c.B, c.Hq, c.Hkv, c.n, P)
     ranks = np.full(turns.shape, 0xFFFF, np.uint16)
@@ -217,7 +218,7 @@ def test_missing_predecessor_times_out_and_context_survives():
                 ranks[t, j] = r
     bad = ranks.copy()
     t = c.n - 1                                   # last tile of head 0 has n contributors
-    bad[t, turns[t, 1]] = 7                       # rank 1 never arrives
+    bad[t, turns[t, 1]] = c.n + 3                 # rank 1 never arrives
     assert dash.sim_check_ranks("shift", c.causal, c.B, c.Hq, c.Hkv, c.n, P, bad) == dash.ERR_DEADLOCK
     dq, dk, dv = (torch.empty(c.B, c.Hq, c.S, c.D, dtype=torch.float32, device="cuda"),
                   torch.empty(c.B, c.Hkv, c.S, c.D, dtype=torch.bfloat16, device="cuda"),
