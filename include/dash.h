@@ -116,6 +116,17 @@ int dash_attn_fwd_window(const dash_bf16* q, const dash_bf16* k, const dash_bf16
  * query tile (shift rotates from query tile kv mod nq; symmetric shift is
  * shift).  Same arguments otherwise (no causal flag), same determinism and
  * errors.
+ *   Key blocks (backward only; the pages give no schedule for more key tiles
+ * than query tiles, where every dQ tile would take one ordered chain of
+ * Skv/128 contributions): when dash_key_blocks returns G > 1 the keys are cut
+ * into G blocks of Skv/G keys.  Block g of head h runs as head h*G + g of one
+ * backward with B*Hq*G heads and Skv/G keys (its K, V, dK and dV rows are the
+ * head's rows g*Skv/G .. (g+1)*Skv/G - 1, used in place; Q, dO, LSE and delta
+ * are copied per block into a library workspace), with the schedule's tasks
+ * and accumulation order of that shape (DASH_SCHED_AUTO then picks for it);
+ * dq = the G blocks' fp32 dQ sums added in ascending block order.  If the
+ * workspace cannot be allocated the call runs unsplit.  The debug entry
+ * (dash_attn_bwd_debug) never splits.
  */
 int dash_attn_bwd_cross(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v,
                         const dash_bf16* o, const dash_bf16* dO, const float* lse,
@@ -168,6 +179,16 @@ int dash_select_schedule(int B, int Hq, int Hkv, int S, int D, int causal);
  * dash_attn_bwd rejects.  Host only; needs no GPU.
  */
 int dash_head_split(int schedule, int causal, int B, int Hq, int Hkv, int S, int D, int window, int Skv, int P);
+
+/*
+ * dash_key_blocks -- the number of key blocks G that dash_attn_bwd_cross
+ * cuts the keys into (no counterpart on the pages): with Hq == Hkv and Skv a
+ * multiple of 128, the largest divisor of Skv/128 that leaves at least
+ * ceil(Sq/128) key tiles per block, so that each dQ tile's ordered chains are
+ * no longer than its query tile count; else 1 (no split).  Returns G >= 1, or
+ * DASH_ERR_ARG for non-positive sizes.  Host only; needs no GPU.
+ */
+int dash_key_blocks(int Hq, int Hkv, int Sq, int Skv);
 
 /*
  * dash_attn_bwd_preprocess -- delta[b,h,s] = sum_d dO[b,h,s,d] * O[b,h,s,d].

@@ -18,8 +18,10 @@ SHAPES = {
     "q256_kv640_d64": (1, 2, 2, 256, 640, 64),        # 2 query tiles, 5 key tiles
     "q640_kv256_d128_gqa": (1, 4, 2, 640, 256, 128),  # 5 query tiles, 2 key tiles
     "q200_kv333_d64_gqa": (2, 2, 1, 200, 333, 64),    # ragged tails on both sides
-    "q130_kv1024_d128": (1, 1, 1, 130, 1024, 128),    # 2 query tiles (2-row tail), 8 key tiles
+    "q130_kv1024_d128": (1, 1, 1, 130, 1024, 128),    # 2 query tiles (2-row tail), 8 key tiles: 4 key blocks
+    "q256_kv1024_d64": (1, 2, 2, 256, 1024, 64),       # 2 query tiles, 8 key tiles: 4 key blocks
 }
+KEY_BLOCKS = {"q130_kv1024_d128": 4, "q256_kv1024_d64": 4}
 _cases = {}
 
 
@@ -89,6 +91,53 @@ def test_cross_order_log_matches_simulator_and_repeats(name, sched):
     hkv = dash.task_heads(sched, False, B, Hq, Hkv, Sq, D, P, Skv=Skv)
     _, turns, _ = dash.sim_schedule(sched, False, B, Hq, hkv, nq, P, nkv=nkv)
     np.testing.assert_array_equal(log.cpu().numpy(), turns)
+    for _ in range(4):
+        again = run_bwd(shape, t, sched)
+        for a, b in zip(first, again):
+            assert same_bits(a, b), sched
+
+
+def _sum_blocks(parts):
+    """fp32 sum in ascending block order, each addition rounded to nearest."""
+    acc = parts[0].clone()
+    for p in parts[1:]:
+        acc = acc + p
+    return acc
+
+
+@pytest.mark.parametrize("name", list(KEY_BLOCKS))
+@pytest.mark.parametrize("sched", ["serialized_ascending", "descending_q"])
+def test_key_blocks_equal_the_blocks_run_one_by_one(name, sched):
+    """With more key tiles than query tiles the backward cuts the keys into
+    blocks, runs them as extra heads of one launch and adds the blocks' dQ
+    sums in ascending block order.  For the schedules whose accumulation
+    order is the KV index (independent of how tasks are dealt), that equals,
+    bit for bit, one call per key block followed by the same fp32 sum, with
+    dK and dV the blocks' own."""
+    shape, t, _, _ = case(name)
+    B, Hq, Hkv, Sq, Skv, D = shape
+    G = KEY_BLOCKS[name]
+    whole = run_bwd(shape, t, sched)
+    L = Skv // G
+    dqs, dks, dvs = [], [], []
+    for g in range(G):
+        tb = dict(t)
+        tb["k"] = t["k"][:, :, g * L:(g + 1) * L].contiguous()
+        tb["v"] = t["v"][:, :, g * L:(g + 1) * L].contiguous()
+        dq, _, dk, dv = run_bwd((B, Hq, Hkv, Sq, L, D), tb, sched)
+        dqs.append(dq)
+        dks.append(dk)
+        dvs.append(dv)
+    assert same_bits(whole[0], _sum_blocks(dqs))
+    assert same_bits(whole[2], torch.cat(dks, dim=2))
+    assert same_bits(whole[3], torch.cat(dvs, dim=2))
+
+
+@pytest.mark.parametrize("name", list(KEY_BLOCKS))
+@pytest.mark.parametrize("sched", SCHEDS[1:])
+def test_key_blocks_repeat_bitwise(name, sched):
+    shape, t, _, _ = case(name)
+    first = run_bwd(shape, t, sched)
     for _ in range(4):
         again = run_bwd(shape, t, sched)
         for a, b in zip(first, again):

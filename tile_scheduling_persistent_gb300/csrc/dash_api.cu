@@ -71,7 +71,7 @@ struct DevBuf {
 constexpr int kIntHeader = 16;
 
 struct Workspace {
-    DevBuf delta, ints, ranks, time, task_start, dbg_ranks, part;
+    DevBuf delta, ints, ranks, time, task_start, dbg_ranks, part, kb;
     long long table_key[8] = {-1, -1, -1, -1, -1, -1, -1, -1};
     void release() {
         delta.release();
@@ -81,6 +81,7 @@ struct Workspace {
         task_start.release();
         dbg_ranks.release();
         part.release();
+        kb.release();
         for (auto& k : table_key) k = -1;
     }
 };
@@ -168,10 +169,11 @@ int head_split_cached(const Shape& g, int P, int D) {
     return v;
 }
 
+// delta_in: delta [B*Hq][S] computed by the caller (o is then not read), or null.
 int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const dash_bf16* o, const dash_bf16* dO,
              const float* lse, float* dq, dash_bf16* dk, dash_bf16* dv, int B, int Hq, int Hkv, int S, int D,
              int causal, int schedule, cudaStream_t stream, const dash_debug_opts* dbg, int window = 0,
-             int Skv = 0) {
+             int Skv = 0, const float* delta_in = nullptr) {
     const void* ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv};
     for (const void* ptr : ptrs)
         if (!aligned16(ptr)) return DASH_ERR_ARG;
@@ -251,7 +253,8 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
     if (cudaMemsetAsync(ints, 0, (size_t)(kIntHeader + (kSubTiles + 1) * tiles) * sizeof(int), stream) != cudaSuccess ||
         cudaMemsetAsync(dq, 0, (size_t)B * Hq * S * D * sizeof(float), stream) != cudaSuccess)
         return DASH_ERR_CUDA;
-    if (launch_preprocess(o, dO, (float*)ws->delta.p, (long long)B * Hq * S, D, stream)) return DASH_ERR_CUDA;
+    if (!delta_in && launch_preprocess(o, dO, (float*)ws->delta.p, (long long)B * Hq * S, D, stream))
+        return DASH_ERR_CUDA;
 
     BwdParams prm;
     memset(&prm, 0, sizeof(prm));
@@ -259,7 +262,7 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
         make_tmap_3d(&prm.tm_v, v, (long long)B * Hkv, Skv, D) || make_tmap_3d(&prm.tm_do, dO, (long long)B * Hq, S, D))
         return DASH_ERR_CUDA;
     prm.lse = lse;
-    prm.delta = (const float*)ws->delta.p;
+    prm.delta = delta_in ? delta_in : (const float*)ws->delta.p;
     prm.dq = dq;
     prm.dk = (__nv_bfloat16*)dk;
     prm.dv = (__nv_bfloat16*)dv;
@@ -316,6 +319,64 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
                   launch_group_sum(prm.part_dv, dv, B, Hkv, Hq / Hkv, Skv, D, stream)))
         return DASH_ERR_CUDA;
     return DASH_OK;
+}
+
+// Key blocks of the backward with more key tiles than query tiles (full mask,
+// as many key/value heads as query heads, whole key tiles): G, the largest
+// divisor of the key tile count that leaves at least as many key tiles per
+// block as query tiles, so that each dQ tile's ordered chain is at most about
+// as long as in a square problem; 1 = no split.
+int key_blocks(int Hq, int Hkv, int Sq, int Skv) {
+    if (Hq != Hkv || Skv % 128 != 0) return 1;
+    const int nq = (Sq + 127) / 128, nkv = Skv / 128;
+    int best = 1;
+    for (int g = 2; g <= nkv; ++g)
+        if (nkv % g == 0 && nkv / g >= nq) best = g;
+    return best;
+}
+
+// The backward with different lengths, the keys cut into G blocks: block g of
+// head h runs as head h*G + g of one backward with B*H*G heads and Skv/G keys
+// (those are the contiguous rows g*Skv/G.. of the head's K, V, dK and dV, so
+// dK and dV are written in place), each with a copy of the head's Q, dO, LSE
+// and delta (delta from the full O and dO); then dq = the G blocks' fp32
+// partial sums added in ascending block order.  Each dQ tile thus takes G
+// ordered chains of Skv/G/128 contributions instead of one of Skv/128.
+// Returns DASH_ERR_NOMEM (nothing launched) when the copies do not fit.
+int bwd_cross_blocks(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const dash_bf16* o,
+                     const dash_bf16* dO, const float* lse, float* dq, dash_bf16* dk, dash_bf16* dv, int B, int H,
+                     int Sq, int Skv, int D, int schedule, cudaStream_t stream, int G) {
+    const void* ptrs[] = {q, k, v, o, dO, lse, dq, dk, dv};
+    for (const void* ptr : ptrs)
+        if (!aligned16(ptr)) return DASH_ERR_ARG;
+    int rc = validate_shape(B, H, H, Sq, D, 0, schedule);
+    if (rc) return rc;
+    if ((long long)B * H * Skv >= (1ll << 31) || (long long)B * H * G * Sq >= (1ll << 31)) return DASH_ERR_ARG;
+    int dev = 0;
+    if ((rc = check_device(&dev))) return rc;
+    const long long BH = (long long)B * H;
+    auto up = [](long long x) { return (x + 255) & ~255ll; };
+    const long long b_x = up(BH * G * Sq * D * 2), b_r = up(BH * G * Sq * 4), b_d = up(BH * Sq * 4);
+    const long long b_q = up(BH * G * Sq * D * 4);
+    Workspace* ws = get_ws(dev, stream);
+    if (ws->kb.ensure((size_t)(2 * b_x + 2 * b_r + b_d + b_q))) return DASH_ERR_NOMEM;
+    char* base = (char*)ws->kb.p;
+    dash_bf16* qv = (dash_bf16*)base;
+    dash_bf16* dov = (dash_bf16*)(base + b_x);
+    float* lsev = (float*)(base + 2 * b_x);
+    float* dlv = (float*)(base + 2 * b_x + b_r);
+    float* delta = (float*)(base + 2 * b_x + 2 * b_r);
+    float* dqv = (float*)(base + 2 * b_x + 2 * b_r + b_d);
+    if (launch_preprocess(o, dO, delta, BH * Sq, D, stream) ||
+        launch_replicate(q, qv, (long long)Sq * D * 2, BH, G, stream) ||
+        launch_replicate(dO, dov, (long long)Sq * D * 2, BH, G, stream) ||
+        launch_replicate(lse, lsev, (long long)Sq * 4, BH, G, stream) ||
+        launch_replicate(delta, dlv, (long long)Sq * 4, BH, G, stream))
+        return DASH_ERR_CUDA;
+    rc = bwd_impl(qv, k, v, o, dov, lsev, dqv, dk, dv, B, H * G, H * G, Sq, D, 0, schedule, stream, nullptr, 0,
+                  Skv / G, dlv);
+    if (rc) return rc;
+    return launch_block_sum(dqv, dq, BH, G, (long long)Sq * D, stream) ? DASH_ERR_CUDA : DASH_OK;
 }
 
 }  // namespace
@@ -439,6 +500,12 @@ int dash_attn_bwd_cross(const dash_bf16* q, const dash_bf16* k, const dash_bf16*
                         const dash_bf16* dO, const float* lse, float* dq, dash_bf16* dk, dash_bf16* dv, int B,
                         int Hq, int Hkv, int Sq, int Skv, int D, int schedule, dash_stream_t stream) {
     if (Skv < 1) return DASH_ERR_ARG;
+    const int G = (Skv != Sq) ? key_blocks(Hq, Hkv, Sq, Skv) : 1;
+    if (G > 1) {
+        const int rc = bwd_cross_blocks(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Sq, Skv, D, schedule,
+                                        (cudaStream_t)stream, G);
+        if (rc != DASH_ERR_NOMEM) return rc;   // else one chain per dQ tile, as below
+    }
     return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, Sq, D, 0, schedule, (cudaStream_t)stream, nullptr, 0,
                     Skv);
 }
@@ -449,6 +516,11 @@ int dash_attn_bwd_window(const dash_bf16* q, const dash_bf16* k, const dash_bf16
     if (window < 1) return DASH_ERR_ARG;
     return bwd_impl(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Hkv, S, D, 1, schedule, (cudaStream_t)stream, nullptr,
                     window);
+}
+
+int dash_key_blocks(int Hq, int Hkv, int Sq, int Skv) {
+    if (Hq <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0) return DASH_ERR_ARG;
+    return Skv != Sq ? key_blocks(Hq, Hkv, Sq, Skv) : 1;
 }
 
 int dash_select_schedule(int B, int Hq, int Hkv, int S, int D, int causal) {

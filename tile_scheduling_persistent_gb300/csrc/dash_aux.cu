@@ -89,6 +89,42 @@ __global__ void __launch_bounds__(256) group_sum_kernel(const float4* __restrict
     }
 }
 
+// ---------------------------------------------------------------- key blocks
+// Inputs of the key-block split of the backward with different query and key
+// lengths: dst[bh][g][e] = src[bh][e] for g < G (T = uint4 when a head's
+// array is a whole number of 16-byte words, else uint32_t).
+template <typename T>
+__global__ void __launch_bounds__(256) replicate_kernel(const T* __restrict__ src, T* __restrict__ dst,
+                                                       long long per_head, int G, long long total) {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < total;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long bh = i / ((long long)G * per_head);
+        const long long e = (i - bh * G * per_head) % per_head;
+        dst[i] = src[bh * per_head + e];
+    }
+}
+
+// out[bh][e] = ((part[bh][0][e] + part[bh][1][e]) + ...) + part[bh][G-1][e]
+// (fp32, round to nearest): the G key blocks' dQ partial sums added in
+// ascending block order.
+__global__ void __launch_bounds__(256) block_sum_kernel(const float4* __restrict__ part, float4* __restrict__ out,
+                                                       long long n4, int G, long long head4) {
+    for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n4;
+         i += (long long)gridDim.x * blockDim.x) {
+        const long long bh = i / head4, r = i - bh * head4;
+        const float4* src = part + bh * G * head4 + r;
+        float4 a = src[0];
+        for (int g = 1; g < G; ++g) {
+            const float4 v = src[(long long)g * head4];
+            a.x = __fadd_rn(a.x, v.x);
+            a.y = __fadd_rn(a.y, v.y);
+            a.z = __fadd_rn(a.z, v.z);
+            a.w = __fadd_rn(a.w, v.w);
+        }
+        out[i] = a;
+    }
+}
+
 // ---------------------------------------------------------------- ranks
 // Model time of a pair = its position in its worker's unit-step sequence
 // (worker = task % P, tasks taken in order); the accumulation rank of KV
@@ -178,6 +214,37 @@ int launch_group_sum(const float* part, void* out, int B, int Hkv, int G, int Sk
     const long long cap = (long long)sms * 8;
     if (blocks > cap) blocks = cap;
     group_sum_kernel<<<(unsigned)blocks, 256, 0, s>>>((const float4*)part, (uint2*)out, n4, G, head4);
+    return cudaGetLastError() == cudaSuccess ? 0 : -2;
+}
+
+namespace {
+long long grid_for(long long n) {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long blocks = (n + 255) / 256, cap = (long long)sms * 8;
+    return blocks < cap ? blocks : cap;
+}
+}  // namespace
+
+int launch_replicate(const void* src, void* dst, long long bytes_per_head, long long BH, int G, cudaStream_t s) {
+    if (BH <= 0 || bytes_per_head <= 0 || bytes_per_head % 4) return -1;
+    if (bytes_per_head % 16 == 0) {
+        const long long per = bytes_per_head / 16, total = BH * G * per;
+        replicate_kernel<uint4><<<(unsigned)grid_for(total), 256, 0, s>>>((const uint4*)src, (uint4*)dst, per, G, total);
+    } else {
+        const long long per = bytes_per_head / 4, total = BH * G * per;
+        replicate_kernel<uint32_t><<<(unsigned)grid_for(total), 256, 0, s>>>((const uint32_t*)src, (uint32_t*)dst, per,
+                                                                             G, total);
+    }
+    return cudaGetLastError() == cudaSuccess ? 0 : -2;
+}
+
+int launch_block_sum(const float* part, float* out, long long BH, int G, long long elems_per_head, cudaStream_t s) {
+    if (elems_per_head % 4) return -1;
+    const long long head4 = elems_per_head / 4, n4 = BH * head4;
+    if (n4 == 0) return 0;
+    block_sum_kernel<<<(unsigned)grid_for(n4), 256, 0, s>>>((const float4*)part, (float4*)out, n4, G, head4);
     return cudaGetLastError() == cudaSuccess ? 0 : -2;
 }
 

@@ -21,6 +21,11 @@ int launch_finalize(const float* src, void* dst, size_t numel, cudaStream_t s);
 // of G query heads in ascending order.
 int load_aux_kernels();   // load the auxiliary backward kernels on the current device
 int launch_group_sum(const float* part, void* out, int B, int Hkv, int G, int Skv, int D, cudaStream_t s);
+// Key-block split of the backward with different query and key lengths:
+// dst [BH][G][bytes_per_head] = G copies of each head's src [BH][bytes_per_head];
+// out fp32 [BH][elems] = part [BH][G][elems] summed over G in ascending order.
+int launch_replicate(const void* src, void* dst, long long bytes_per_head, long long BH, int G, cudaStream_t s);
+int launch_block_sum(const float* part, float* out, long long BH, int G, long long elems_per_head, cudaStream_t s);
 // Accumulation ranks of a static schedule, built on the device:
 // ranks [B*Hq*n][n] (uint16), scratch `time` [B*Hq*n][n] (uint32),
 // `task_start` [num_tasks] (uint32).

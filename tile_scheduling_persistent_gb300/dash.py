@@ -27,7 +27,7 @@ EXPORTS = (
     "dash_release_workspaces", "dash_num_ctas", "dash_sim_schedule", "dash_sim_check_ranks",
     "dash_attn_bwd_debug", "dash_debug_tile_probe", "dash_attn_bwd_noalloc", "dash_select_schedule",
     "dash_attn_fwd", "dash_sim_schedule_band", "dash_attn_bwd_window", "dash_attn_fwd_window",
-    "dash_sim_schedule_cross", "dash_attn_bwd_cross", "dash_attn_fwd_cross", "dash_head_split",
+    "dash_sim_schedule_cross", "dash_attn_bwd_cross", "dash_attn_fwd_cross", "dash_head_split", "dash_key_blocks",
     "dash_noalloc_init", "dash_get_status_noalloc",
 )
 
@@ -245,6 +245,14 @@ def head_split(schedule, causal, B, Hq, Hkv, S, D, P, window=None, Skv=None):
                                int(Skv or 0), int(P))
     _check(rc if rc < 0 else 0, "dash_head_split")
     return rc == 1
+
+
+def key_blocks(Hq, Hkv, Sq, Skv):
+    """The number of key blocks the backward with key length Skv != Sq cuts
+    the keys into (see dash_key_blocks); 1 = no split."""
+    rc = lib().dash_key_blocks(int(Hq), int(Hkv), int(Sq), int(Skv))
+    _check(rc if rc < 0 else 0, "dash_key_blocks")
+    return rc
 
 
 def task_heads(schedule, causal, B, Hq, Hkv, S, D, P, window=None, Skv=None):
