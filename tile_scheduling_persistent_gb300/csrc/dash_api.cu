@@ -187,8 +187,9 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
     if (Skv < 0 || (Skv != S && (causal || (dbg && dbg->ranks_host))) || (Skv + 127) / 128 > 65535 ||
         (long long)B * Hkv * Skv >= (1ll << 31))
         return DASH_ERR_ARG;   // different lengths: full mask only
-    // auto: different lengths run descending Q (measured best for 1K queries x 8K keys on GB300:
-    // descending 153, ascending 148, shift 85 TFLOP/s); otherwise the shape table
+    // auto: different lengths run descending Q (with one ordered chain per dQ tile, measured best for 1K
+    // queries x 8K keys on GB300: descending 153, ascending 148, shift 85 TFLOP/s; the key-block path of
+    // dash_attn_bwd_cross calls this with the square block shape, where the shape table applies)
     if (schedule == kAuto) schedule = (Skv != S) ? kDescending : select_schedule(D, causal);
     int dev = 0;
     if ((rc = check_device(&dev))) return rc;
