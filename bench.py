@@ -250,7 +250,7 @@ def time_schedule(w, sched, tensors, outs, steps, warmup, stream, kernel_events=
     # preprocess + persistent kernel + finalize, and the two group sums (dK,
     # dV) when the shape runs one task per query head; with key blocks
     # (different lengths) four input copies and the block sum as well
-    if w.Skv and w.Skv != w.S and dash.key_blocks(w.Hq, w.Hkv, w.S, w.Skv) > 1:
+    if w.Skv and w.Skv != w.S and dash.key_blocks(w.B, w.Hq, w.Hkv, w.S, w.Skv) > 1:
         return ms, kms, 8
     split = dash.head_split(sched, w.causal, w.B, w.Hq, w.Hkv, w.S, w.D, dash.num_ctas(), w.window, w.Skv)
     return ms, kms, 3 + (2 if split else 0)

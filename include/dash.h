@@ -184,11 +184,12 @@ int dash_head_split(int schedule, int causal, int B, int Hq, int Hkv, int S, int
  * dash_key_blocks -- the number of key blocks G that dash_attn_bwd_cross
  * cuts the keys into (no counterpart on the pages): with Hq == Hkv and Skv a
  * multiple of 128, the largest divisor of Skv/128 that leaves at least
- * ceil(Sq/128) key tiles per block, so that each dQ tile's ordered chains are
- * no longer than its query tile count; else 1 (no split).  Returns G >= 1, or
- * DASH_ERR_ARG for non-positive sizes.  Host only; needs no GPU.
+ * ceil(Sq/128) key tiles per block (so that each dQ tile's ordered chains are
+ * no longer than its query tile count) and keeps B*Hq*G*Sq < 2^31; else 1 (no
+ * split).  Returns G >= 1, or DASH_ERR_ARG for non-positive sizes.  Host
+ * only; needs no GPU.
  */
-int dash_key_blocks(int Hq, int Hkv, int Sq, int Skv);
+int dash_key_blocks(int B, int Hq, int Hkv, int Sq, int Skv);
 
 /*
  * dash_attn_bwd_preprocess -- delta[b,h,s] = sum_d dO[b,h,s,d] * O[b,h,s,d].

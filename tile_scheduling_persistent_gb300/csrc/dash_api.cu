@@ -326,13 +326,14 @@ int bwd_impl(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v, const d
 // as many key/value heads as query heads, whole key tiles): G, the largest
 // divisor of the key tile count that leaves at least as many key tiles per
 // block as query tiles, so that each dQ tile's ordered chain is at most about
-// as long as in a square problem; 1 = no split.
-int key_blocks(int Hq, int Hkv, int Sq, int Skv) {
+// as long as in a square problem, and keeps the block shape's B*Hq*G*Sq
+// within the index range; 1 = no split.
+int key_blocks(int B, int Hq, int Hkv, int Sq, int Skv) {
     if (Hq != Hkv || Skv % 128 != 0) return 1;
     const int nq = (Sq + 127) / 128, nkv = Skv / 128;
     int best = 1;
     for (int g = 2; g <= nkv; ++g)
-        if (nkv % g == 0 && nkv / g >= nq) best = g;
+        if (nkv % g == 0 && nkv / g >= nq && (long long)B * Hq * g * Sq < (1ll << 31)) best = g;
     return best;
 }
 
@@ -352,7 +353,7 @@ int bwd_cross_blocks(const dash_bf16* q, const dash_bf16* k, const dash_bf16* v,
         if (!aligned16(ptr)) return DASH_ERR_ARG;
     int rc = validate_shape(B, H, H, Sq, D, 0, schedule);
     if (rc) return rc;
-    if ((long long)B * H * Skv >= (1ll << 31) || (long long)B * H * G * Sq >= (1ll << 31)) return DASH_ERR_ARG;
+    if ((long long)B * H * Skv >= (1ll << 31) || (long long)B * H * G * Sq >= (1ll << 31)) return DASH_ERR_ARG;   // key_blocks keeps G below
     int dev = 0;
     if ((rc = check_device(&dev))) return rc;
     const long long BH = (long long)B * H;
@@ -501,7 +502,7 @@ int dash_attn_bwd_cross(const dash_bf16* q, const dash_bf16* k, const dash_bf16*
                         const dash_bf16* dO, const float* lse, float* dq, dash_bf16* dk, dash_bf16* dv, int B,
                         int Hq, int Hkv, int Sq, int Skv, int D, int schedule, dash_stream_t stream) {
     if (Skv < 1) return DASH_ERR_ARG;
-    const int G = (Skv != Sq) ? key_blocks(Hq, Hkv, Sq, Skv) : 1;
+    const int G = (Skv != Sq && B > 0 && Hq > 0 && Sq > 0) ? key_blocks(B, Hq, Hkv, Sq, Skv) : 1;
     if (G > 1) {
         const int rc = bwd_cross_blocks(q, k, v, o, dO, lse, dq, dk, dv, B, Hq, Sq, Skv, D, schedule,
                                         (cudaStream_t)stream, G);
@@ -519,9 +520,9 @@ int dash_attn_bwd_window(const dash_bf16* q, const dash_bf16* k, const dash_bf16
                     window);
 }
 
-int dash_key_blocks(int Hq, int Hkv, int Sq, int Skv) {
-    if (Hq <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0) return DASH_ERR_ARG;
-    return Skv != Sq ? key_blocks(Hq, Hkv, Sq, Skv) : 1;
+int dash_key_blocks(int B, int Hq, int Hkv, int Sq, int Skv) {
+    if (B <= 0 || Hq <= 0 || Hkv <= 0 || Sq <= 0 || Skv <= 0) return DASH_ERR_ARG;
+    return Skv != Sq ? key_blocks(B, Hq, Hkv, Sq, Skv) : 1;
 }
 
 int dash_select_schedule(int B, int Hq, int Hkv, int S, int D, int causal) {

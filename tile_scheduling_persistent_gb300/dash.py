@@ -247,10 +247,10 @@ def head_split(schedule, causal, B, Hq, Hkv, S, D, P, window=None, Skv=None):
     return rc == 1
 
 
-def key_blocks(Hq, Hkv, Sq, Skv):
+def key_blocks(B, Hq, Hkv, Sq, Skv):
     """The number of key blocks the backward with key length Skv != Sq cuts
     the keys into (see dash_key_blocks); 1 = no split."""
-    rc = lib().dash_key_blocks(int(Hq), int(Hkv), int(Sq), int(Skv))
+    rc = lib().dash_key_blocks(int(B), int(Hq), int(Hkv), int(Sq), int(Skv))
     _check(rc if rc < 0 else 0, "dash_key_blocks")
     return rc
 
