@@ -64,21 +64,19 @@ __device__ __forceinline__ bool wait1(uint32_t bar, uint32_t parity, const Ctl& 
     return true;
 }
 
-// Whole-warp bounded wait with a warp-uniform outcome: lane 0 polls, then
-// every lane observes the completed phase itself (acquire per thread).
+// Whole-warp bounded wait with a warp-uniform outcome: lane 0 polls (its
+// try_wait acquires the phase), the outcome is broadcast, and the warp
+// barrier orders every other lane's later accesses after lane 0's acquire.
 // kFast: first one try_wait by every lane and a vote, which returns at once
 // when the phase has already completed (one shared-memory round trip instead
-// of three); the polled path only when it has not.
+// of two); the polled path only when it has not.
 template <bool kFast = false>
 __device__ __forceinline__ bool waitw(uint32_t bar, uint32_t parity, const Ctl& c, int role, int i0, int site) {
     if (kFast && __all_sync(0xffffffffu, ptx::mbar_try_wait(bar, parity))) return true;
     int ok = 1;
     if ((threadIdx.x & 31) == 0) ok = wait1(bar, parity, c, role, i0, site) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok) {
-        while (!ptx::mbar_try_wait(bar, parity)) {
-        }
-    }
+    __syncwarp();
     return ok != 0;
 }
 

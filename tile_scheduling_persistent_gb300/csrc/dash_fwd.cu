@@ -111,15 +111,25 @@ __device__ bool fwait1(uint32_t bar, uint32_t parity, const FwdWait& w, int role
     return true;
 }
 
+// Every lane's own poll after lane 0 saw the phase complete: normally no
+// iteration at all; bounded all the same (role + 8 in the status if it runs out).
+__device__ __noinline__ int fwait_lanes(uint32_t bar, uint32_t parity, const FwdWait& w, int role, int i0) {
+    for (int n = 0; !ptx::mbar_try_wait(bar, parity); ++n) {
+        if (n == (1 << 24)) {
+            fwd_timeout(w, role + 8, i0);
+            return 0;
+        }
+    }
+    return 1;
+}
+
 // Whole warp: lane 0 polls, then every lane observes the phase (acquire).
-__device__ bool fwaitw(uint32_t bar, uint32_t parity, const FwdWait& w, int role, int i0) {
+__device__ __forceinline__ bool fwaitw(uint32_t bar, uint32_t parity, const FwdWait& w, int role, int i0) {
     int ok = 1;
     if ((threadIdx.x & 31) == 0) ok = fwait1(bar, parity, w, role, i0) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
-    if (ok)
-        while (!ptx::mbar_try_wait(bar, parity)) {
-        }
-    return ok != 0;
+    if (ok && !ptx::mbar_try_wait(bar, parity)) ok = fwait_lanes(bar, parity, w, role, i0);
+    return __all_sync(0xffffffffu, ok != 0);
 }
 
 // kMasked: compiled for a partial last tile (S % 128 != 0) or a sliding
@@ -358,10 +368,10 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
             __syncwarp();
             if (lane == 0) ptx::mbar_arrive(BAR(F_P_READY + buf));
         }
-        // The last S this thread saw was committed after PV(nkv-3): step through
-        // the phases of PV(nkv-2) and PV(nkv-1) so that parity cannot alias.
-        for (int jj = (nkv > 2 ? nkv - 2 : 0); ok && jj < nkv; ++jj)
-            ok = fwaitw(BAR(F_O_DONE), (uint32_t)(jj & 1), fw, 3, nkv);
+        // O is complete once every MMA is: F_DRAIN, committed once after the
+        // last one, has a single phase, so this wait cannot alias (a wait on
+        // O_DONE could see its parity pass on between two lanes' polls)
+        if (ok) ok = fwaitw(BAR(F_DRAIN), 0u, fw, 3, nkv);
         if (ok) {
             ptx::tc_fence_after();
             const bool row_ok = !kMasked || qt * 128 + row < p.S;   // rows past S are not stored (loads stay warp-wide)
