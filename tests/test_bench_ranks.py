@@ -69,3 +69,14 @@ def test_one_process_needs_no_group():
     assert r.max(3) == 3.0
     assert r.pick_fastest({"x": 2.0, "y": 1.0}) == "y"
     assert r.rate(4.0, 2.0) == pytest.approx(2000.0)
+
+
+def test_pick_fastest_keeps_the_preferred_schedule_within_the_margin():
+    sys.path.insert(0, ROOT)
+    import bench
+    r = bench.Ranks()
+    trials = {"symmetric_shift": 8.6867, "shift": 8.6792, "descending_q": 14.3}
+    assert r.pick_fastest(trials) == "shift"
+    assert r.pick_fastest(trials, prefer="symmetric_shift") == "symmetric_shift"
+    assert r.pick_fastest({"a": 10.0, "b": 9.0}, prefer="a") == "b"   # 11% slower: not kept
+    assert r.pick_fastest({"a": 10.0, "b": 9.0}, prefer="zzz") == "b"
