@@ -28,6 +28,16 @@ SHAPES = {
     "full_s130_d128": (1, 1, 1, 130, 128, False),
     "causal_s100_d64": (1, 1, 1, 100, 64, True),
 }
+# More than twice as many Q tiles (CTAs) as a GB300 has SMs, so the grid runs
+# in several waves (uneven tile lengths on causal masks, a ragged tail, a
+# window), each against the oracle and repeated bit for bit.
+MANY = {
+    # name: (B, Hq, Hkv, S, D, causal, window)
+    "full_b2_h16_s1280_d64": (2, 16, 16, 1280, 64, False, None),
+    "causal_b2_h16_s1280_d128_gqa": (2, 16, 4, 1280, 128, True, None),
+    "causal_b2_h16_s1200_d64_gqa_ragged": (2, 16, 8, 1200, 64, True, None),
+    "window_b2_h16_s1280_d128_w300": (2, 16, 16, 1280, 128, True, 300),
+}
 LSE_ABS = 1e-4   # fp32 LSE of O(10): the kernel's fp32 score sums against the exact fp64 value
 
 
@@ -50,6 +60,40 @@ def test_forward_parity(name):
     o, lse = forward(q.to(dev), k.to(dev), v.to(dev), causal)
     check(name + " o", o, o_ref)
     assert np.abs(lse.cpu().numpy().astype(np.float64) - lse_ref).max() <= LSE_ABS
+
+
+@pytest.mark.parametrize("name", list(MANY))
+def test_forward_parity_many_tiles(name):
+    B, Hq, Hkv, S, D, causal, window = MANY[name]
+    assert B * Hq * ((S + 127) // 128) > 2 * 152
+    q, k, v, _ = make_qkvdo(B, Hq, Hkv, S, D, seed=8)
+    o_ref, lse_ref = A.attn_fwd(q, k, v, causal, window=window)
+    dev = torch.device("cuda")
+    q, k, v = q.to(dev), k.to(dev), v.to(dev)
+    o = torch.empty_like(q)
+    lse = torch.empty(B, Hq, S, dtype=torch.float32, device=dev)
+    dash.attn_fwd(q, k, v, o, lse, causal, window=window)
+    code, info = dash.get_status()
+    assert code == 0, (code, info)
+    check(name + " o", o, o_ref)
+    assert np.abs(lse.cpu().numpy().astype(np.float64) - lse_ref).max() <= LSE_ABS
+    o2 = torch.empty_like(o)
+    lse2 = torch.empty_like(lse)
+    dash.attn_fwd(q, k, v, o2, lse2, causal, window=window)
+    assert same_bits(o, o2) and same_bits(lse, lse2)
+
+
+def test_forward_rescaling_many_tiles():
+    # sigma 3 scores (frequent in-loop rescaling of O) with 320 Q tiles
+    B, Hq, Hkv, S, D, causal = 2, 16, 16, 1280, 64, False
+    q, k, _, _ = make_qkvdo(B, Hq, Hkv, S, D, seed=5, sigma_qkv=3.0)
+    _, _, v, _ = make_qkvdo(B, Hq, Hkv, S, D, seed=7)
+    o_ref, lse_ref = A.attn_fwd(q, k, v, causal)
+    dev = torch.device("cuda")
+    o, lse = forward(q.to(dev), k.to(dev), v.to(dev), causal)
+    check("o", o, o_ref)
+    rel = np.abs(lse.cpu().numpy().astype(np.float64) - lse_ref) / np.maximum(np.abs(lse_ref), 1.0)
+    assert rel.max() <= 1e-5
 
 
 def test_forward_large_scores_need_rescaling():
