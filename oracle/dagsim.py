@@ -174,17 +174,21 @@ def make_tasks(schedule: str, B: int, Hq: int, Hkv: int, n: int, causal: bool, b
                 for j in range(n if nkv is None else nkv):
                     tasks.append([Pair(b, hq, i, j) for hq in heads
                                   for i in visit_q(schedule, n, causal, j, band)])
-    if schedule == "shift" and causal and band is None:
+    # a band that reaches every tile of the causal triangle visits what the
+    # causal mask visits, and is dealt like it
+    banded = band is not None and band < n
+    if schedule == "shift" and causal and not banded:
         # causal shift is dealt KV-tile-major: task k is KV tile k // (B*Hkv) of
         # head group k % (B*Hkv), so that each wave holds tiles of similar length
         groups = B * Hkv
         tasks = [tasks[g * n + j] for j in range(n) for g in range(groups)]
-    elif schedule in STATIC and band is None and nkv is None and (not causal or schedule == "symmetric_shift"):
-        # shift on a full mask and symmetric shift (full or causal) are dealt by
-        # the parity of the task's tile (pair) index: the even tiles of every
-        # head group first, then the odd ones.  Within a wave a dQ tile then
-        # receives a contribution every second step of the rotation instead of
-        # every step, while the task -> worker rule stays k -> k mod P.
+    elif schedule in STATIC and nkv is None and (banded or not causal or schedule == "symmetric_shift"):
+        # shift on a full mask or a band, and symmetric shift (full or causal),
+        # are dealt by the parity of the task's tile (pair) index: the even
+        # tiles of every head group first, then the odd ones.  Within a wave a
+        # dQ tile then receives a contribution every second step of the
+        # rotation instead of every step, while the task -> worker rule stays
+        # k -> k mod P.
         groups = B * Hkv
         T = len(tasks) // groups
         tasks = [tasks[g * T + t] for par in range(2) for g in range(groups) for t in range(par, T, 2)]

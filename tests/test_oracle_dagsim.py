@@ -256,21 +256,23 @@ def test_band_wide_enough_is_causal():
         assert a.turn == b.turn
 
 
-@pytest.mark.parametrize("schedule,causal,n", [("shift", False, 8), ("symmetric_shift", True, 16),
-                                               ("symmetric_shift", False, 6)])
-def test_parity_dealing_spaces_a_tiles_contributions_two_steps_apart(schedule, causal, n):
-    # Full-mask shift and symmetric shift deal the even tiles (pairs) of every
-    # head group first, then the odd ones; with one wave per parity class, the
-    # contributions a dQ tile receives from one wave are at least two steps of
-    # the rotation apart (head-major dealing would give one every step).
+@pytest.mark.parametrize("schedule,causal,n,band", [("shift", False, 8, None), ("symmetric_shift", True, 16, None),
+                                                    ("symmetric_shift", False, 6, None), ("shift", True, 12, 4),
+                                                    ("symmetric_shift", True, 9, 3)])
+def test_parity_dealing_spaces_a_tiles_contributions_two_steps_apart(schedule, causal, n, band):
+    # Full-mask shift, banded shift and symmetric shift deal the even tiles
+    # (pairs) of every head group first, then the odd ones; with one wave per
+    # parity class, the contributions a dQ tile receives from one wave are at
+    # least two steps of the rotation apart (head-major dealing would give one
+    # every step).
     B, H = 1, 4
-    s = G.build(schedule, B, H, H, n, causal, P=10 ** 6)
+    s = G.build(schedule, B, H, H, n, causal, P=10 ** 6, band=band)
     T = len(s.tasks) // (B * H)
     even = (T + 1) // 2
     for k, t in enumerate(s.tasks):
         parity = 0 if k < B * H * even else 1
         tiles = {p.j for p in t}
-        if schedule == "shift":
+        if schedule == "shift" or band is not None:
             assert tiles == {(k % even) * 2 + parity if parity == 0 else ((k - B * H * even) % (T // 2)) * 2 + 1}
     for par in range(2):
         wave = [k for k in range(len(s.tasks)) if (k < B * H * even) == (par == 0)]

@@ -93,17 +93,21 @@ DASH_HD int first_kv(const Shape& s, int q) { return (s.causal && s.win && q >= 
 //    round-robin in that order gives every wave tiles of nearly equal length
 //    (busiest of 152 workers at 1.035x the mean instead of 1.09x for B1 H32
 //    S16384) and spaces the contributions to a dQ tile about a wave apart.
-//  - Shift on a full mask and symmetric shift (full or causal), with equal
-//    query and key lengths and no window, are parity-major: the even tiles
-//    (pairs) of every head group, head group by head group, then the odd
-//    ones.  All of a head's tiles in one wave would add into each of its dQ
-//    tiles at every step of the rotation; a wave of one parity adds at every
-//    second step, which leaves each ordered link two steps to complete.
+//  - Shift on a full mask or a sliding-window band, and symmetric shift
+//    (full or causal; on a band it is shift), with equal query and key
+//    lengths, are parity-major: the even tiles (pairs) of every head group,
+//    head group by head group, then the odd ones.  All of a head's tiles in
+//    one wave would add into each of its dQ tiles at every step of the
+//    rotation; a wave of one parity adds at every second step, which leaves
+//    each ordered link two steps to complete.
 //  - Everything else is head-group-major (tile k % T of group k / T).
-DASH_HD bool kv_major(const Shape& s) { return s.sched == kShift && s.causal && !s.win; }
+// (A band with win >= n visits every tile of the causal triangle and is dealt
+// as the causal mask is.)
+DASH_HD bool banded(const Shape& s) { return s.win && s.win < s.n; }
+DASH_HD bool kv_major(const Shape& s) { return s.sched == kShift && s.causal && !banded(s); }
 DASH_HD bool parity_major(const Shape& s) {
-    return !s.win && !s.nk && (s.sched == kShift || s.sched == kSymmetric) &&
-           (!s.causal || s.sched == kSymmetric);
+    return !s.nk && (s.sched == kShift || s.sched == kSymmetric) &&
+           (!s.causal || banded(s) || s.sched == kSymmetric);
 }
 
 // A task's tile (or symmetric pair) and head group (b * Hkv + hkv); callers
