@@ -42,10 +42,10 @@ METRIC = "deterministic attn-bwd TFLOP/s & % of BF16 peak; det/nondet throughput
 # of the kernel source it was taken on.  A figure is reported only while the
 # kernel source still has that hash; otherwise the roofline's traffic is null.
 NCU_TRAFFIC = {
-    ("full_b4_h16_s4096_d128", "shift"): (687127296 + 362092544, "3ceabc427d7382ad"),
-    ("causal_b4_h16_s8192_d128", "symmetric_shift"): (1470986240 + 844288768, "3ceabc427d7382ad"),
-    ("causal_b1_h32_s16384_d64", "shift"): (3681160960 + 1866800896, "3ceabc427d7382ad"),
-    ("gqa_causal_b1_hq32_hkv8_s16384_d128", "symmetric_shift"): (1437229312 + 1194093568, "3ceabc427d7382ad"),
+    ("full_b4_h16_s4096_d128", "shift"): (687872000 + 361767424, "81632c474664975f"),
+    ("causal_b4_h16_s8192_d128", "symmetric_shift"): (1474869760 + 847471104, "81632c474664975f"),
+    ("causal_b1_h32_s16384_d64", "shift"): (3644788480 + 1830926848, "81632c474664975f"),
+    ("gqa_causal_b1_hq32_hkv8_s16384_d128", "symmetric_shift"): (1429513216 + 1189779712, "81632c474664975f"),
 }
 KERNEL_SOURCES = ("tile_scheduling_persistent_gb300/csrc/dash_bwd.cu",
                   "tile_scheduling_persistent_gb300/csrc/dash_bwd.cuh",
