@@ -638,12 +638,14 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                 // every query head is its own task (fp32 partial, summed later)
                 const size_t grow = ((size_t)(d.b * p.Hkv + d.hkv) * p.Skv + (size_t)d.kv * 128 + krow) * D;
                 const uint32_t col = half == 0 ? C::COL_DK : C::COL_DV;
+                // The epilogue runs once per KV tile: its column loop stays
+                // rolled, which keeps it out of the instruction cache's way.
                 if constexpr (D == 128) {
                     // bf16 dK / dV, or the fp32 partials of one query head
                     const bool f32 = p.part_dk != nullptr;
                     uint8_t* outb = f32 ? reinterpret_cast<uint8_t*>((half == 0 ? p.part_dk : p.part_dv) + grow)
                                         : reinterpret_cast<uint8_t*>((half == 0 ? p.dk : p.dv) + grow);
-#pragma unroll
+#pragma unroll 1
                     for (int cc = 0; cc < D / 32; ++cc) {
                         uint32_t v[32];
                         ptx::tmem_ld16(tmem + kv_lanes + col + 32 * cc, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
@@ -672,7 +674,7 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
                 } else {
                     // D = 64: always one task per key/value head group, bf16 out
                     __nv_bfloat16* out = (half == 0 ? p.dk : p.dv) + grow;
-#pragma unroll
+#pragma unroll 1
                     for (int cc = 0; cc < D / 32; ++cc) {
                         uint32_t v[32];
                         ptx::tmem_ld16(tmem + kv_lanes + col + 32 * cc, *reinterpret_cast<uint32_t(*)[16]>(&v[0]));

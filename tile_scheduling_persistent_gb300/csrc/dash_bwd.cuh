@@ -201,13 +201,18 @@ struct BwdParams {
 
 // ------------------------------------------------------------------ MMA issue
 // All operand addresses are shared-window byte addresses of 1024-aligned
-// 128-row boxes.
+// 128-row boxes.  One thread issues.  kUnroll: the backward keeps the K-step
+// loops rolled (1): with its five products (and their call sites) unrolled,
+// its code no longer fits the SM's instruction cache (about 26% of the
+// requests missed and instruction fetch was the second-largest stall), and
+// the extra issue cycles hide behind each 512-cycle product.  The forward,
+// whose code fits, unrolls them.
 
-template <int D>
+template <int D, int kUnroll = 1>
 __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t sA, uint32_t sB) {
     // [128 x 128] = A[128 x D] * B[128 x D]^T, both K-major
     constexpr uint32_t idesc = ptx::idesc_bf16(128, 128, 0, 0);
-#pragma unroll
+#pragma unroll kUnroll
     for (int kk = 0; kk < D / 16; ++kk) {
         const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
         ptx::mma_ss(d_tmem, ptx::sdesc(sA + off, 16, 1024), ptx::sdesc(sB + off, 16, 1024), idesc,
@@ -215,12 +220,12 @@ __device__ __forceinline__ void issue_s(uint32_t d_tmem, uint32_t sA, uint32_t s
     }
 }
 
-template <int D>
+template <int D, int kUnroll = 1>
 __device__ __forceinline__ void issue_dv(uint32_t d_tmem, uint32_t p_tmem, uint32_t sDo,
                                          uint32_t acc) {
     // dV[128 x D] (+)= P^T[128 x 128] (tmem, K-major) * dO[128 x D] (MN-major)
     constexpr uint32_t idesc = ptx::idesc_bf16(128, D, 0, 1);
-#pragma unroll
+#pragma unroll kUnroll
     for (int kk = 0; kk < 8; ++kk) {
         const uint32_t a = p_tmem + (kk >> 2) * 64 + (kk & 3) * 8;
         ptx::mma_ts(d_tmem, a, ptx::sdesc(sDo + kk * 2048, kBox, 1024), idesc, acc | (kk > 0));
@@ -231,7 +236,7 @@ template <int D>
 __device__ __forceinline__ void issue_dk(uint32_t d_tmem, uint32_t sDsT, uint32_t sQ, uint32_t acc) {
     // dK[128 x D] (+)= dS^T[128 x 128] (K-major) * Q[128 x D] (MN-major)
     constexpr uint32_t idesc = ptx::idesc_bf16(128, D, 0, 1);
-#pragma unroll
+#pragma unroll 1
     for (int kk = 0; kk < 8; ++kk) {
         const uint32_t aoff = (kk >> 2) * kBox + (kk & 3) * 32;
         ptx::mma_ss(d_tmem, ptx::sdesc(sDsT + aoff, 16, 1024), ptx::sdesc(sQ + kk * 2048, kBox, 1024),
@@ -243,7 +248,7 @@ template <int D>
 __device__ __forceinline__ void issue_dq(uint32_t d_tmem, uint32_t sDsT, uint32_t sK) {
     // dQ[128 x D] = dS[128 x 128] (dS^T read MN-major) * K[128 x D] (MN-major)
     constexpr uint32_t idesc = ptx::idesc_bf16(128, D, 1, 1);
-#pragma unroll
+#pragma unroll 1
     for (int kk = 0; kk < 8; ++kk) {
         ptx::mma_ss(d_tmem, ptx::sdesc(sDsT + kk * 2048, kBox, 1024),
                     ptx::sdesc(sK + kk * 2048, kBox, 1024), idesc, kk > 0);

@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
             bool ok = fwait1(BAR(F_Q_FULL), 0, fw, 2, 0) && fwait1(BAR(F_K_FULL), 0, fw, 2, 0);
             if (ok) {
                 ptx::tc_fence_after();
-                issue_s<D>(tS(0), sQ, sK(0));
+                issue_s<D, D / 16>(tS(0), sQ, sK(0));
                 ptx::tc_commit(BAR(F_S_FULL));
                 ptx::tc_commit(BAR(F_K_EMPTY));
             }
@@ -245,14 +245,14 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
                     // S(j+1) overwrites the buffer PV(j-1) read; MMAs run in issue order
                     if (!fwait1(BAR(F_K_FULL + ((j + 1) & 1)), (uint32_t)(((j + 1) / 2) & 1), fw, 2, j)) break;
                     ptx::tc_fence_after();
-                    issue_s<D>(tS(j + 1), sQ, sK(j + 1));
+                    issue_s<D, D / 16>(tS(j + 1), sQ, sK(j + 1));
                     ptx::tc_commit(BAR(F_S_FULL + ((j + 1) & 1)));
                     ptx::tc_commit(BAR(F_K_EMPTY + ((j + 1) & 1)));
                 }
                 if (!fwait1(BAR(F_P_READY + (j & 1)), (uint32_t)((j / 2) & 1), fw, 2, j)) break;
                 if (!fwait1(BAR(F_V_FULL + (j & 1)), (uint32_t)((j / 2) & 1), fw, 2, j)) break;
                 ptx::tc_fence_after();
-                issue_dv<D>(tmem + C::COL_O, tS(j), sV(j), j > 0 ? 1u : 0u);   // O (+)= P V_j
+                issue_dv<D, 8>(tmem + C::COL_O, tS(j), sV(j), j > 0 ? 1u : 0u);   // O (+)= P V_j
                 ptx::tc_commit(BAR(F_V_EMPTY + (j & 1)));
                 ptx::tc_commit(BAR(F_O_DONE));
             }
