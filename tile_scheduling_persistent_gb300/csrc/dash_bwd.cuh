@@ -281,12 +281,16 @@ __device__ __forceinline__ void softmax_64(uint32_t tmem_s_lane, int c0, float l
         uint32_t r[32];
         ptx::tmem_ld32(tmem_s_lane + c0 + 32 * h, r);
         ptx::tmem_ld_wait();
-        const float lsrc = h ? lse2_b : lse2_a;
+        // -LSE of the columns (negated once, exactly), broadcast two at a
+        // time; the exponent scale*log2e*S - LSE as one packed fma per pair
+        const float nsrc = -(h ? lse2_b : lse2_a);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            const float l = __shfl_sync(0xffffffffu, lsrc, k);
-            const float x = ptx::ex2(fmaf(__uint_as_float(r[k]), scale_log2e, -l));
-            P[32 * h + k] = (!kBranchMask && diag && row > c0 + 32 * h + k) ? 0.f : x;
+        for (int k = 0; k < 32; k += 2) {
+            const ptx::f2 nl{__shfl_sync(0xffffffffu, nsrc, k), __shfl_sync(0xffffffffu, nsrc, k + 1)};
+            const ptx::f2 y = ptx::fma2({__uint_as_float(r[k]), __uint_as_float(r[k + 1])}, {scale_log2e, scale_log2e}, nl);
+            const float x0 = ptx::ex2(y.x), x1 = ptx::ex2(y.y);
+            P[32 * h + k] = (!kBranchMask && diag && row > c0 + 32 * h + k) ? 0.f : x0;
+            P[32 * h + k + 1] = (!kBranchMask && diag && row > c0 + 32 * h + k + 1) ? 0.f : x1;
         }
         if (kBranchMask && mask) {
 #pragma unroll
@@ -323,11 +327,11 @@ __device__ __forceinline__ void ds_64(uint32_t tmem_dp_lane, int c0, float delta
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const int a = 16 * q4 + 2 * k;
-            const float e0 = __shfl_sync(0xffffffffu, dsrc, (a & 31));
-            const float e1 = __shfl_sync(0xffffffffu, dsrc, (a & 31) + 1);
-            const float d0 = P[a] * (__uint_as_float(r[2 * k]) - e0) * scale;
-            const float d1 = P[a + 1] * (__uint_as_float(r[2 * k + 1]) - e1) * scale;
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(d0, d1);
+            const ptx::f2 e{__shfl_sync(0xffffffffu, dsrc, (a & 31)), __shfl_sync(0xffffffffu, dsrc, (a & 31) + 1)};
+            // (P * (dP - delta)) * scale, in that order, two columns per instruction
+            const ptx::f2 d = ptx::mul2(ptx::mul2({P[a], P[a + 1]}, ptx::sub2({__uint_as_float(r[2 * k]), __uint_as_float(r[2 * k + 1])}, e)),
+                                        {scale, scale});
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(d.x, d.y);
             pk[k] = *reinterpret_cast<uint32_t*>(&h2);
         }
 #pragma unroll
