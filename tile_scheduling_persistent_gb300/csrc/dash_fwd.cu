@@ -327,10 +327,16 @@ __global__ void __launch_bounds__(256, 1) dash_fwd_kernel(const __grid_constant_
             const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;   // P = 0, not NaN, for such a row
 #pragma unroll
             for (int i = 0; i < 8; ++i) part[i] = 0.f;
+            // the exponents and the partial sums two columns per instruction
+            // (packed fp32 pairs round each lane as the scalar ops would)
 #pragma unroll
-            for (int k = 0; k < 128; ++k) {
-                x[k] = ptx::ex2(fmaf(x[k], c, -m_use));
-                part[k & 7] += x[k];
+            for (int k = 0; k < 128; k += 2) {
+                const ptx::f2 y = ptx::fma2({x[k], x[k + 1]}, {c, c}, {-m_use, -m_use});
+                x[k] = ptx::ex2(y.x);
+                x[k + 1] = ptx::ex2(y.y);
+                const ptx::f2 s = ptx::add2({part[k & 7], part[(k + 1) & 7]}, {x[k], x[k + 1]});
+                part[k & 7] = s.x;
+                part[(k + 1) & 7] = s.y;
             }
             const float rs = ((part[0] + part[1]) + (part[2] + part[3])) + ((part[4] + part[5]) + (part[6] + part[7]));
             l = l * alpha + rs;

@@ -304,6 +304,17 @@ __device__ __forceinline__ f2 fma2(f2 a, f2 b, f2 c) {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
     return r;
 }
+__device__ __forceinline__ f2 add2(f2 a, f2 b) {
+    uint64_t d;
+    asm("{\n\t.reg .b64 a, b;\n\t"
+        "mov.b64 a, {%1, %2};\n\tmov.b64 b, {%3, %4};\n\t"
+        "add.rn.f32x2 %0, a, b;\n\t}"
+        : "=l"(d)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    f2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
+    return r;
+}
 __device__ __forceinline__ f2 sub2(f2 a, f2 b) {
     uint64_t d;
     asm("{\n\t.reg .b64 a, b;\n\t"
