@@ -502,9 +502,11 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
     } else {
         if constexpr (Regs<D>::kDrain < kRegsLaunch) ptx::setmaxnreg_dec<Regs<D>::kDrain>();   // 96 at D = 128: as launched
         // ================================================== dQ drain + ordered reduction + dK/dV epilogue
-        // Fast-path waits here only at D = 64: at D = 128 a drain that reaches
-        // its turn sooner lengthens the ordered chain (measured 5-9% slower).
-        constexpr bool kDrainFast = (D == 64);
+        // Fast-path waits (every lane tries once, then a vote) at both head
+        // dimensions: once the kernel's hot code fitted the instruction cache
+        // they measured +0.5% ordered and +5% unordered at D = 128 (with the
+        // unrolled MMA loops they had cost the ordered schedules 5-9%).
+        constexpr bool kDrainFast = true;
         const int sub = warp & 3;
         const int half = (wg == 4) ? 1 : 0;
         const int st = 2 * sub + half;                     // dQ sub-tile: rows 16*st .. 16*st+15
