@@ -421,9 +421,8 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
         // Per-column statistics of a pair's Q tile: lane l holds LSE and delta
         // of columns c0+l and c0+32+l (columns past S of a partial last tile
         // read 0 and are masked).
-        // sv: LSE of the two columns (times log2(e) at D = 64, where the
-        // values are used at once), then their delta.
-        constexpr bool kAhead = (D == 128);
+        // sv: LSE of the two columns, then their delta.
+        constexpr bool kAhead = true;
         constexpr float kLseMul = kAhead ? 1.f : kLog2e;
         auto fetch = [&](const PairDesc& fd, float (&sv)[4]) {
             const int qcol = fd.q * 128 + c0 + lane;
@@ -434,11 +433,12 @@ __global__ void __launch_bounds__(kThreads, 1) dash_bwd_kernel(const __grid_cons
             sv[2] = va ? ptx::ld_nc(p.delta + qrow) : 0.f;
             sv[3] = vb ? ptx::ld_nc(p.delta + qrow + 32) : 0.f;
         };
-        // At D = 128 the next pair's descriptor is read at the top of this
-        // pair and its statistics are loaded after this pair's P phase, so
-        // that the shared-memory read and the global loads overlap the dP wait
-        // and the dS phase; at D = 64 (measured faster there) a pair's
-        // descriptor and statistics are read at the top of its own iteration.
+        // kAhead: the next pair's descriptor is read at the top of this pair
+        // and its statistics are loaded after this pair's P phase, so that the
+        // shared-memory read and the global loads overlap the dP wait and the
+        // dS phase (both head dimensions on the current kernel; the other
+        // order reads a pair's descriptor and statistics at the top of its
+        // own iteration).
         PairDesc d{};
         float sv[4] = {0.f, 0.f, 0.f, 0.f};
         if constexpr (kAhead) {
