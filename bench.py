@@ -42,10 +42,10 @@ METRIC = "deterministic attn-bwd TFLOP/s & % of BF16 peak; det/nondet throughput
 # of the kernel source it was taken on.  A figure is reported only while the
 # kernel source still has that hash; otherwise the roofline's traffic is null.
 NCU_TRAFFIC = {
-    ("full_b4_h16_s4096_d128", "shift"): (683953920 + 358560768, "6197d3de6a4f87c2"),
-    ("causal_b4_h16_s8192_d128", "symmetric_shift"): (1437945856 + 813625344, "6197d3de6a4f87c2"),
-    ("causal_b1_h32_s16384_d64", "shift"): (4255566848 + 2243081472, "6197d3de6a4f87c2"),
-    ("gqa_causal_b1_hq32_hkv8_s16384_d128", "symmetric_shift"): (1399942400 + 1170601472, "6197d3de6a4f87c2"),
+    ("full_b4_h16_s4096_d128", "shift"): (685323264 + 358591744, "1cdafb619ba4f4f7"),
+    ("causal_b4_h16_s8192_d128", "symmetric_shift"): (1433069568 + 810143232, "1cdafb619ba4f4f7"),
+    ("causal_b1_h32_s16384_d64", "shift"): (4205477376 + 2210018816, "1cdafb619ba4f4f7"),
+    ("gqa_causal_b1_hq32_hkv8_s16384_d128", "symmetric_shift"): (1382528768 + 1162282496, "1cdafb619ba4f4f7"),
 }
 KERNEL_SOURCES = ("tile_scheduling_persistent_gb300/csrc/dash_bwd.cu",
                   "tile_scheduling_persistent_gb300/csrc/dash_bwd.cuh",
