@@ -1,6 +1,6 @@
-// dash_ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarrier, TMA
-// (cp.async.bulk / cp.async.bulk.tensor), tcgen05 (MMA, TMEM alloc/ld/st,
-// commit, fences), and gpu-scope acquire/release.
+// dash_ptx.cuh -- thin inline-PTX wrappers for sm_103a: mbarrier, TMA tile
+// loads (cp.async.bulk.tensor), tcgen05 (MMA, TMEM alloc/ld/st, commit,
+// fences), packed fp32 pair arithmetic, and gpu-scope acquire/release.
 //
 // Operand layouts used by this library (all 128-byte swizzled, bf16):
 //   a "box" is 128 rows x 64 elements (128 B per row, 16 KiB), written by a
@@ -95,14 +95,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
 }
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
-                                          uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-            dst),
-        "l"(src), "r"(bytes), "r"(bar)
-        : "memory");
-}
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
@@ -110,22 +102,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// TMA reduce-add of a 2D box from shared memory into global memory (bulk
-// async-group completion), and the bulk async-group waits.
-__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, int c0, int c1, uint32_t src) {
-    asm volatile(
-        "cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map),
-        "r"(c0), "r"(c1), "r"(src)
-        : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Wait until the shared-memory sources of every committed bulk group were read.
-__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
-// Wait until every committed bulk group has completed (its writes performed).
-__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void fence_proxy_async_global() {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-}
 
 // ---------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
@@ -362,10 +338,6 @@ __device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, 
     asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
                  "f"(d)
                  : "memory");
-}
-// Named barrier among `nthreads` threads (ids 1..15; 0 is __syncthreads).
-__device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 }  // namespace ptx
