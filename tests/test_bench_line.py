@@ -61,3 +61,24 @@ def test_library_arm_line():
     assert e2e["value"] > 0 and e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
     # delta, the persistent kernel and the finalize per timed step at least
     assert line["gpu_launches"] >= 3 * line["steps"]
+
+
+def test_traffic_is_reported_only_for_the_kernel_source_it_was_taken_on(monkeypatch):
+    # the roofline's DRAM traffic comes from an ncu capture keyed to the kernel
+    # sources' hash: a figure is reported while the sources still have that
+    # hash and withheld (null) once they change
+    import sys
+    sys.path.insert(0, ROOT)
+    import bench
+    h = bench.kernel_source_hash()
+    assert len(h) == 16 and int(h, 16) >= 0
+    assert bench.NCU_TRAFFIC, "no recorded captures"
+    for (w, s), (nbytes, src) in bench.NCU_TRAFFIC.items():
+        assert nbytes > 0
+        assert bench.traffic_for(w, s) == (nbytes if src == h else None)
+    w, s = next(iter(bench.NCU_TRAFFIC))
+    monkeypatch.setitem(bench.NCU_TRAFFIC, (w, s), (123, h))
+    assert bench.traffic_for(w, s) == 123
+    monkeypatch.setitem(bench.NCU_TRAFFIC, (w, s), (123, "0" * 16))
+    assert bench.traffic_for(w, s) is None
+    assert bench.traffic_for("no_such_workload", "shift") is None
